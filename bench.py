@@ -1,0 +1,475 @@
+#!/usr/bin/env python3
+"""Benchmark of the split-KV paged decode/verify path on GB300.
+
+One step = one pass of the whole hot path over one batch: plan (the cache is
+reset first, as at the start of a forward), split-KV attention, LSE merge.
+The default workload is the uniform MTP verify batch: 16 sequences x 119000
+tokens, 4 query tokens each, 32 query / 2 KV heads, head_dim 128, bf16 pages
+of 16 tokens behind a random block table (1.95 GB of K/V per call, larger
+than L2, so no flush is needed between steps).
+
+Metric: effective KV-read TB/s = K/V bytes of the batch / time per step
+(higher is better); the JSON line also carries microseconds per call.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--config I]
+
+Under torchrun (N > 1) every rank runs its own copy of the batch on its own
+GPU (weak scaling: work items are independent, no collective on the data
+path); the timed region is bracketed by barriers and the max over ranks is
+reported.  ``--impl reference`` times the fp64 CPU oracle on the host cores
+on bounded samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import sk_inputs as si  # noqa: E402
+
+METRIC = "decode-attention us/call and effective KV-read TB/s vs GB300 HBM peak"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="sk", choices=["sk", "reference"])
+    ap.add_argument("--config", type=int, default=2, help="workload 1..5 (default 2)")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fixed-split", action="store_true", help="time the fixed split instead of the plan")
+    return ap.parse_args()
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _config_json(w, extra=None):
+    cfg = {"workload": w.name, "batch": w.bs, "seq_lens_total": int(w.seq_lens.sum()),
+           "q_len": int(w.max_q_len), "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
+           "head_dim": w.head_dim, "page": w.page, "kv_dtype": "fp8_e4m3" if w.kv_dtype else "bf16",
+           "kv_bytes_per_call": w.kv_bytes, "num_sms_plan": w.num_sms, "seg_max": w.seg_max,
+           "l2": "inputs larger than L2 (K/V %.2f GB per call), no flush" % (w.kv_bytes / 1e9)
+           if w.kv_bytes > 129e6 else "L2 flushed (256 MB write) before every step"}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def _oracle_units(w, q_host_bits, kv_gather, rng, seconds):
+    """Times the fp64 oracle on whole (sequence, KV head) units of ``w`` until
+    ``seconds`` of CPU time have passed.  kv_gather(s) -> host page bits of sequence s."""
+    from oracle import oracle
+    units = [(s, h) for s in range(w.bs) if w.seq_lens[s] > 0 and w.q_lens[s] > 0
+             for h in range(w.num_kv_heads)]
+    order = rng.permutation(len(units))
+    cu = w.cu_q
+    done_bytes, elapsed, n = 0, 0.0, 0
+    cache = {}
+    for k in order:
+        s, h = units[k]
+        L, qs = int(w.seq_lens[s]), int(w.q_lens[s])
+        if s not in cache:
+            cache.clear()
+            cache[s] = kv_gather(s)
+        kv_bits = cache[s]
+        npg = (L + w.page - 1) // w.page
+        bt = np.arange(npg, dtype=np.int32)[None, :]
+        rows = np.array([j * w.num_q_heads + h * w.group + i for j in range(qs) for i in range(w.group)],
+                        dtype=np.int64)
+        qb = q_host_bits[cu[s]:cu[s] + qs]
+        t0 = time.perf_counter()
+        oracle.attention(qb, kv_bits, w.kv_dtype, w.k_scale, w.v_scale, bt, w.page,
+                         np.array([L], np.int32), np.array([0, qs], np.int32), w.num_q_heads,
+                         w.num_kv_heads, w.head_dim, w.sm_scale, w.causal, rows=rows)
+        elapsed += time.perf_counter() - t0
+        done_bytes += L * 2 * w.head_dim * w.elem_bytes
+        n += 1
+        if elapsed >= seconds:
+            break
+    return done_bytes, elapsed, n
+
+
+def _host_inputs(w):
+    """Host copies of the workload's inputs, generated on the CPU with the same seeds."""
+    import torch
+    q = si.make_q(w, "cpu")
+    q_bits = q.view(torch.int16).numpy().view(np.uint16)
+
+    def gather(s):
+        L = int(w.seq_lens[s])
+        npg = (L + w.page - 1) // w.page
+        return _kv_pages_cpu(w, w.block_table[s, :npg])
+    return q_bits, gather
+
+
+_KV_CPU = {}
+
+
+def _kv_pages_cpu(w, blocks):
+    import torch
+    key = w.name
+    if key not in _KV_CPU:
+        _KV_CPU.clear()
+        _KV_CPU[key] = si.make_kv(w, "cpu")
+    kv = _KV_CPU[key][torch.as_tensor(blocks.astype(np.int64))]
+    return kv.numpy() if w.kv_dtype == si.KV_FP8 else kv.view(torch.int16).numpy().view(np.uint16)
+
+
+def _cpu_baseline(w, seconds, seed=0, from_device=None):
+    from oracle import oracle
+    rng = np.random.default_rng(seed)
+    if from_device is not None:
+        q_bits, gather = from_device
+    else:
+        q_bits, gather = _host_inputs(w)
+    nbytes, el, n = _oracle_units(w, q_bits, gather, rng, seconds)
+    return {"value": nbytes / el / 1e12, "unit": "TB/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{n} (sequence, KV head) units of {w.name}: all G*q query rows over the whole "
+                      f"sequence, {nbytes / 1e6:.1f} MB of K/V in {el:.2f} s, fp64 C oracle, OpenMP"}
+
+
+def run_reference(a, w, rank):
+    if rank != 0:
+        return 0
+    from oracle import oracle
+    oracle.build()
+    q_bits, gather = _host_inputs(w)
+    rng = np.random.default_rng(7)
+    per_step = max(1.0, min(6.0, 150.0 / max(1, a.steps + a.warmup)))
+    for _ in range(a.warmup):
+        _oracle_units(w, q_bits, gather, rng, per_step / 4)
+    tot_b, tot_t, tot_n = 0, 0.0, 0
+    for _ in range(a.steps):
+        b, t, n = _oracle_units(w, q_bits, gather, rng, per_step)
+        tot_b += b
+        tot_t += t
+        tot_n += n
+    val = tot_b / tot_t / 1e12
+    sample = (f"each step: (sequence, KV head) units of {w.name} for ~{per_step:.1f} s of oracle time; "
+              f"{tot_n} units, {tot_b / 1e6:.1f} MB of K/V over {a.steps} steps")
+    line = {"metric": METRIC, "value": val, "unit": "TB/s", "n_gpus": a.gpus, "steps": a.steps,
+            "warmup": a.warmup, "ms_per_step": 1e3 * tot_t / a.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference", "config": _config_json(w),
+            "cpu_baseline": {"value": val, "unit": "TB/s", "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": val, "unit": "TB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "20", "-f", self.path],
+                                         stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        busy = [s for s, p in zip(sm, pw) if p > 1.15 * min(pw)] if pw else sm
+        return {"sm_mhz": statistics.median(busy or sm), "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(pw) if pw else None}
+
+
+# ----------------------------------------------------------------------------- roofline helpers
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "of measured"
+    return FALLBACK_HBM_GBS, "of fallback"
+
+
+def _kernel_sources_sha():
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "paged_split_kv_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _ncu_traffic(workload, sha):
+    """DRAM bytes per attention launch from the committed ncu summary, if it was
+    taken on the current kernel sources (else None)."""
+    for f in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
+        text = open(f).read()
+        if f"workload: {workload}" not in text or f"source_sha: {sha}" not in text:
+            continue
+        for line in text.splitlines():
+            if line.strip().startswith("dram_bytes_per_launch:"):
+                try:
+                    return int(float(line.split(":", 1)[1].strip()))
+                except ValueError:
+                    return None
+    return None
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_sk(a, w, ws, rank, local):
+    import torch
+    import paged_split_kv_gb300 as sk
+    if not os.path.exists(sk.LIB_PATH):
+        from paged_split_kv_gb300 import build as b
+        b.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    q = si.make_q(w, dev)
+    kv = si.make_kv(w, dev)
+    bt = torch.as_tensor(w.block_table, device=dev)
+    lens = torch.as_tensor(w.seq_lens, device=dev)
+    cu = torch.as_tensor(w.cu_q, device=dev)
+    use_plan = not a.fixed_split
+    nsm = w.num_sms
+    hkv = w.num_kv_heads
+    nt = w.num_tokens
+    plan = torch.empty(sk.plan_capacity(w.bs, hkv, nsm), dtype=torch.int32, device=dev) if use_plan else None
+    tok = torch.empty(nt, dtype=torch.int32, device=dev) if use_plan else None
+    part_o = torch.empty((nt, w.seg_max, w.num_q_heads, w.head_dim), dtype=torch.float32, device=dev)
+    part_m = torch.empty((nt, w.seg_max, w.num_q_heads), dtype=torch.float32, device=dev)
+    part_l = torch.empty((nt, w.seg_max, w.num_q_heads), dtype=torch.float32, device=dev)
+    out = torch.empty((nt, w.num_q_heads, w.head_dim), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((nt, w.num_q_heads), dtype=torch.float32, device=dev)
+    fixed = 0 if use_plan else sk.sk_fixed_nseg(w.bs, hkv, nsm, w.seg_max)
+    flush = None if w.kv_bytes > 129e6 else torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if flush is not None:
+            flush.fill_(1)
+        if ev is not None:
+            ev[0].record(stream)
+        if use_plan:
+            sk.sk_plan_cache_reset()
+            sk.sk_build_plan(lens, cu, hkv, plan, tok, nsm, w.seg_max, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        sk.sk_paged_decode_attn(q, kv, bt, lens, cu, plan, part_o, part_m, part_l,
+                                max_q_len=w.max_q_len, sm_scale=w.sm_scale, num_sms=nsm,
+                                k_scale=w.k_scale, v_scale=w.v_scale, causal=bool(w.causal),
+                                stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+        sk.sk_merge_segments(part_o, part_m, part_l, tok, out, lse, fixed_nseg=fixed, stream=stream)
+        if ev is not None:
+            ev[3].record(stream)
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    for _ in range(max(3, a.warmup)):
+        step()
+    torch.cuda.synchronize()
+    status = sk.sk_get_device_status(clear=True)
+    if status:
+        raise RuntimeError(f"device status {status:#x} after warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(a.steps)]
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    for i in range(a.steps):
+        step(evs[i])
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    if ws > 1:
+        torch.distributed.barrier()
+    plan_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    attn_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    merge_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    total_ms = evs[0][0].elapsed_time(evs[-1][3])
+    if ws > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / a.steps
+    value = ws * w.kv_bytes * a.steps / (total_ms * 1e-3) / 1e12
+
+    # end to end through the public call with host inputs (pinned), copies inside the region
+    e2e = None
+    if a.e2e_steps > 0:
+        host = {"q": q.cpu().pin_memory(), "kv": kv.cpu().pin_memory(), "bt": bt.cpu().pin_memory(),
+                "lens": lens.cpu().pin_memory(), "cu": cu.cpu().pin_memory()}
+        dq, dkv = torch.empty_like(q), torch.empty_like(kv)
+        dbt, dlens, dcu = torch.empty_like(bt), torch.empty_like(lens), torch.empty_like(cu)
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        wsp = {}
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+
+        def e2e_step():
+            dq.copy_(host["q"], non_blocking=True)
+            dkv.copy_(host["kv"], non_blocking=True)
+            dbt.copy_(host["bt"], non_blocking=True)
+            dlens.copy_(host["lens"], non_blocking=True)
+            dcu.copy_(host["cu"], non_blocking=True)
+            sk.sk_plan_cache_reset()
+            o, l = sk.paged_decode_attention(dq, dkv, dbt, dlens, dcu, max_q_len=w.max_q_len,
+                                             sm_scale=w.sm_scale, num_sms=nsm, k_scale=w.k_scale,
+                                             v_scale=w.v_scale, causal=bool(w.causal),
+                                             seg_max=w.seg_max, use_plan=use_plan, workspace=wsp)
+            out_h.copy_(o, non_blocking=True)
+            lse_h.copy_(l, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if ws > 1:
+            torch.distributed.barrier()
+        e0.record()
+        for _ in range(a.e2e_steps):
+            e2e_step()
+        e1.record()
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1)
+        if ws > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        assert torch.equal(out_h, out.cpu()), "end-to-end output differs from the device-resident run"
+        e2e = {"value": ws * w.kv_bytes * a.e2e_steps / (e2e_ms * 1e-3) / 1e12, "unit": "TB/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": e2e_ms / a.e2e_steps}
+        del host, dq, dkv
+
+    if rank != 0:
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+
+    attn_avg = statistics.mean(attn_ms)
+    peak, peak_kind = _peaks()
+    q_bytes = nt * w.num_q_heads * w.head_dim * 2
+    # algorithmic bytes of one attention launch: K/V once, Q once, partials written
+    rows_written = int(sum(int(w.q_lens[s]) * w.num_q_heads for s in range(w.bs)))
+    nseg_items = None
+    if use_plan:
+        p_np = plan.cpu().numpy()
+        tok_np = tok.cpu().numpy()
+        nseg_items = int((p_np[1:] >= 0).sum())
+        part_bytes = int(sum(int(tok_np[t]) for t in range(nt))) * w.num_q_heads * (w.head_dim + 2) * 4
+    else:
+        part_bytes = rows_written * fixed * (w.head_dim + 2) * 4
+    attn_bytes = w.kv_bytes + q_bytes + part_bytes
+    achieved = attn_bytes / (attn_avg * 1e-3) / 1e9
+    sha = _kernel_sources_sha()
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                "traffic": _ncu_traffic(w.name, sha), "kernel": "sk attention (split-KV, paged)",
+                "algorithmic_bytes_per_launch": int(attn_bytes), "source_sha": sha}
+
+    cpu = None
+    if not a.no_cpu_baseline and ws == 1:
+        q_bits = q.view(torch.int16).cpu().numpy().view(np.uint16)
+
+        def gather(s):
+            L = int(w.seq_lens[s])
+            npg = (L + w.page - 1) // w.page
+            idx = torch.as_tensor(w.block_table[s, :npg].astype(np.int64), device=dev)
+            sub = kv.index_select(0, idx).cpu()
+            return sub.numpy() if w.kv_dtype == si.KV_FP8 else sub.view(torch.int16).numpy().view(np.uint16)
+        cpu = _cpu_baseline(w, a.cpu_seconds, from_device=(q_bits, gather))
+
+    line = {"metric": METRIC, "value": round(value, 4), "unit": "TB/s", "n_gpus": ws, "steps": a.steps,
+            "warmup": a.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.kv_dtype == si.KV_BF16 else "fp8_e4m3",
+            "data": "synthetic (seeded N(0,1) Q/K/V, random-permuted block table)",
+            "config": _config_json(w, {"split": "plan" if use_plan else "fixed",
+                                       "work_items": nseg_items}),
+            "us_per_call": round(1e3 * statistics.mean([x + y for x, y in zip(attn_ms, merge_ms)]), 2),
+            "us_attention": round(1e3 * attn_avg, 2), "us_merge": round(1e3 * statistics.mean(merge_ms), 2),
+            "us_plan": round(1e3 * statistics.mean(plan_ms), 2),
+            "kv_tbps_attention_plus_merge": round(w.kv_bytes / (1e-3 * statistics.mean(
+                [x + y for x, y in zip(attn_ms, merge_ms)])) / 1e12, 4),
+            "frac_of_8tbps_nominal": round(value / 8.0, 4),
+            "roofline": roofline, "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu,
+            "gpu_launches": a.steps * (3 if use_plan else 2)}
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    a = _args()
+    ws, rank, local = _dist()
+    w = si.config(a.config)
+    if a.impl == "reference":
+        return run_reference(a, w, rank)
+    return run_sk(a, w, ws, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

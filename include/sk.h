@@ -1,0 +1,193 @@
+/*
+ * sk.h -- C ABI of libsk: length-aware split-KV paged decode/verify attention
+ * for one GB300 (sm_103a).
+ *
+ * The method (SGLang PR 39172, "[AMD] gfx950 assembly attention: length-aware
+ * split-KV for dynamic workload") runs in three device steps per attention
+ * call:
+ *   1. sk_build_plan        picks one segment length T from the batch's
+ *                           sequence lengths and writes a compact work list
+ *                           of (sequence, segment) items plus a per-query-
+ *                           token segment count (Modifications, first item).
+ *   2. sk_paged_decode_attn one CTA per (sequence, segment, kv head) work item
+ *                           gathers K/V from standard pages and emits a
+ *                           partial softmax state per query row
+ *                           (Modifications, second item).
+ *   3. sk_merge_segments    merges each token's segments by log-sum-exp,
+ *                           reading only that token's segment count
+ *                           (Modifications, third item).
+ * A NULL plan selects the fixed split of the Motivation section (used for
+ * bs == 1, where it already gives 64 segments).
+ *
+ * Conventions for every call:
+ *  - Pointers marked "device" are device memory owned by the caller; the
+ *    library keeps no reference after the call returns.  It allocates no
+ *    device memory of its own except one status word per device (a static
+ *    __device__ variable).
+ *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
+ *    legacy default stream).  No call synchronises, so the whole path can be
+ *    captured into a CUDA graph.
+ *  - Invalid arguments are caught on the host before anything is launched
+ *    and return a negative sk_status; sk_last_error() then describes the
+ *    problem.  Conditions only the device can see (a block id outside
+ *    [0, num_blocks), a query length above max_q_len, an inconsistent
+ *    cu_seqlens_q) set bits in the device status word and the affected work
+ *    is skipped; read them with sk_get_device_status().
+ *  - Supported shapes: head_dim == 128, page_size == 16, 1 <= bs <= 32767
+ *    (so seq << 16 stays positive), num_q_heads % num_kv_heads == 0.
+ */
+#ifndef SK_H_
+#define SK_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SK_OK = 0,
+    SK_CACHED = 1,            /* sk_build_plan: cache hit, nothing launched */
+    SK_ERR_INVALID = -1,      /* bad pointer, size or stride */
+    SK_ERR_CAPACITY = -2,     /* plan_capacity too small */
+    SK_ERR_UNSUPPORTED = -3,  /* shape outside the supported set */
+    SK_ERR_CUDA = -4,         /* a CUDA runtime call failed */
+    SK_ERR_TIMEOUT = -5       /* reserved: a device wait gave up */
+} sk_status;
+
+typedef enum {
+    SK_KV_BF16 = 0,           /* pages hold bf16 */
+    SK_KV_FP8_E4M3 = 1        /* pages hold OCP e4m3fn codes (vLLM RFC 59111, Proposed Change:
+                                 OCP e4m3fn, not MI300's fnuz), value = code * scale */
+} sk_kv_dtype;
+
+/* Bits of the device status word (sk_get_device_status). */
+#define SK_DEV_BAD_BLOCK 0x1   /* a block-table entry outside [0, num_blocks) was skipped */
+#define SK_DEV_BAD_SEQ 0x2     /* q_len > max_q_len, L > block_table_stride * page, or bad cu_seqlens_q */
+#define SK_DEV_TIMEOUT 0x4     /* a bounded wait inside a kernel expired; its work item was abandoned */
+
+/* Tokens per plan tile.  The plan counts segment lengths in tiles:
+ * plan[0] = tiles per segment, so a segment spans plan[0] * sk_tile_tokens()
+ * tokens (SGLang PR 39172, Modifications: "tiles per segment come from
+ * plan[0]").  Returns 64. */
+int sk_tile_tokens(void);
+
+/* Segment count of the fixed split (SGLang PR 39172, Motivation):
+ * max(1, min(seg_max, pow2floor(num_sms / (bs * num_kv_heads)))), pow2floor
+ * of a value below 1 being 0.  Host-only arithmetic. */
+int sk_fixed_nseg(int bs, int num_kv_heads, int num_sms, int seg_max);
+
+/* Build the length-aware plan on the device (SGLang PR 39172, Modifications).
+ *
+ *   tiles_s = ceil(seq_lens[s] / sk_tile_tokens())
+ *   B       = floor(num_sms / num_kv_heads)
+ *   T       = smallest t >= 1 with sum_s ceil(tiles_s / t) <= B and
+ *             max_s ceil(tiles_s / t) <= seg_max; if no t qualifies (more
+ *             non-empty sequences than B) T = max_s tiles_s, one segment per
+ *             non-empty sequence; T = 1 when every sequence is empty.
+ *
+ * Outputs (device, caller-owned):
+ *   plan     int32[plan_capacity]: plan[0] = T; plan[1+k] = (s << 16) | g for
+ *            every segment g < ceil(tiles_s / T) of every sequence s, in
+ *            (s ascending, g ascending) order; -1 in every later slot.
+ *   tok_nseg int32[num_tokens]: tok_nseg[t] = segment count of t's sequence.
+ * Inputs (device): seq_lens int32[bs] (KV length including this step's query
+ *   tokens), cu_seqlens_q int32[bs+1] (query-token offsets, cu[bs] ==
+ *   num_tokens).
+ * plan_capacity must be >= 1 + max(B, bs); larger values are allowed.
+ *
+ * Plan cache: the plan is built once per forward and reused by every layer.
+ * The cache key is (seq_lens, seq_lens_version, cu_seqlens_q,
+ * cu_seqlens_q_version, bs, num_tokens, num_kv_heads, num_sms, seg_max, plan,
+ * plan_capacity, tok_nseg, whether `stream` is capturing).  A hit returns
+ * SK_CACHED and launches nothing: the caller's plan/tok_nseg buffers still hold
+ * the result.  The version arguments let a caller mark in-place changes (the
+ * Python binding passes tensor._version).  sk_plan_cache_reset() clears the
+ * cache; call it at the start of every forward.
+ * Returns SK_OK (plan kernel enqueued), SK_CACHED, or a negative sk_status. */
+int sk_build_plan(const int32_t *seq_lens, uint64_t seq_lens_version,
+                  const int32_t *cu_seqlens_q, uint64_t cu_seqlens_q_version,
+                  int bs, int num_tokens, int num_kv_heads, int num_sms, int seg_max,
+                  int32_t *plan, int plan_capacity, int32_t *tok_nseg, void *stream);
+
+/* Clear the plan cache (SGLang PR 39172, Modifications: the cache is cleared
+ * at the start of every forward). */
+void sk_plan_cache_reset(void);
+
+/* Number of plan kernels launched by this process so far (cache misses). */
+long long sk_plan_launch_count(void);
+
+/* Split-KV paged attention (SGLang PR 39172, Modifications, second item).
+ *
+ * Grid: with a plan, (plan_capacity - 1) * num_kv_heads CTAs; CTA b takes
+ * work item i = b / num_kv_heads and KV head h = b % num_kv_heads, reads
+ * w = plan[1+i], and exits at once when w == -1.  Sequence s = w >> 16,
+ * segment g = w & 0xFFFF covers keys [g*T, min((g+1)*T, L_s)) with
+ * T = plan[0] * sk_tile_tokens().  With plan == NULL the fixed split runs:
+ * nseg = sk_fixed_nseg(bs, num_kv_heads, num_sms, seg_max) segments per
+ * sequence of ceil(tiles_s / nseg) tiles each (trailing ones may be empty);
+ * the grid is bs * nseg * num_kv_heads.
+ *
+ * Layouts (device):
+ *   q            bf16 [num_tokens, num_q_heads, head_dim], token-major via
+ *                cu_seqlens_q.  Query head hq uses KV head hq / G, G =
+ *                num_q_heads / num_kv_heads.
+ *   kv_pages     [num_blocks, num_kv_heads, page_size, 2*head_dim]: standard
+ *                pages (vLLM RFC 59111, Background): per head, each token
+ *                row holds K in [0, D) and V in [D, 2D).  bf16 or e4m3fn.
+ *   block_table  int32 [bs, block_table_stride]; key p of sequence s lives in
+ *                block block_table[s*stride + p/page_size], row p % page_size.
+ *   seq_lens, cu_seqlens_q as for sk_build_plan; plan as written by it.
+ * Masking: with causal != 0, query token j of sequence s (q_s tokens) sees
+ *   keys p <= L_s - q_s + j; otherwise all L_s keys.
+ * Scores: sm_scale * k_scale * <q, k>; values are multiplied by v_scale (the
+ *   two scales apply to fp8 pages only and are ignored for bf16).
+ * max_q_len: an upper bound on every q_s; it sizes the kernel's row tile
+ *   (rows per work item = G * q_s).
+ * Outputs (device, fp32): for every query token t of the item's sequence,
+ *   every query head hq of KV head h, and the item's segment g:
+ *     part_m[(t*seg_max + g)*num_q_heads + hq]  reference value m (score units)
+ *     part_l[same]                               l = sum_p exp(score_p - m)
+ *     part_o[same * head_dim + d]                o = v_scale * sum_p exp(score_p - m) * V_p[d]
+ *   over the keys of the segment that the row sees.  A row that sees none of
+ *   them gets (m, l, o) = (-inf, 0, 0).  m is not required to be the maximum
+ *   score; m + log(l) and o / l are the segment's unique log-sum-exp and output.
+ *   Arrays are [num_tokens, seg_max, num_q_heads(, head_dim)]; only segments
+ *   that exist are written.
+ * Returns SK_OK or a negative sk_status. */
+int sk_paged_decode_attn(const void *q, const void *kv_pages, int kv_dtype, float k_scale,
+                         float v_scale, const int32_t *block_table, int block_table_stride,
+                         int num_blocks, int page_size, const int32_t *seq_lens,
+                         const int32_t *cu_seqlens_q, const int32_t *plan, int plan_capacity,
+                         int bs, int num_tokens, int max_q_len, int num_q_heads, int num_kv_heads,
+                         int head_dim, float sm_scale, int causal, int num_sms, int seg_max,
+                         float *part_o, float *part_m, float *part_l, void *stream);
+
+/* Merge segment partials by log-sum-exp (SGLang PR 39172, Modifications,
+ * third item: the reduce reads only its token's segment count).
+ * For token t and query head hq with n = tok_nseg[t] (or fixed_nseg when
+ * tok_nseg == NULL) segments, over segments with l > 0:
+ *   M = max m_g,  Lambda = sum l_g exp(m_g - M),
+ *   out = sum o_g exp(m_g - M) / Lambda   (bf16, round to nearest even),
+ *   lse = M + log(Lambda)                  (fp32, optional).
+ * No contributing segment: out = 0, lse = -inf.
+ * out bf16 [num_tokens, num_q_heads, head_dim]; lse fp32 [num_tokens,
+ * num_q_heads] or NULL.  Partials as written by sk_paged_decode_attn.
+ * Returns SK_OK or a negative sk_status. */
+int sk_merge_segments(const float *part_o, const float *part_m, const float *part_l,
+                      const int32_t *tok_nseg, int fixed_nseg, int num_tokens, int num_q_heads,
+                      int head_dim, int seg_max, void *out, float *lse, void *stream);
+
+/* Synchronise `stream`, return the device status word of the current device
+ * (a mask of SK_DEV_* bits, 0 when clean) and clear it when `clear` != 0.
+ * Returns a negative sk_status if a CUDA call fails. */
+int sk_get_device_status(void *stream, int clear);
+
+/* Message for the last negative status returned on this thread. */
+const char *sk_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SK_H_ */

@@ -71,6 +71,8 @@ def _load():
         lib.sko_attention_split.argtypes = common + [P, P, i32, i32, P, P, P, P, P]
         lib.sko_merge.restype = None
         lib.sko_merge.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, P, P]
+        lib.sko_num_threads.restype = i32
+        lib.sko_num_threads.argtypes = []
         _lib = lib
         return lib
 
@@ -81,6 +83,11 @@ def _ptr(a: Optional[np.ndarray]):
 
 def _c(a, dtype) -> np.ndarray:
     return np.ascontiguousarray(np.asarray(a, dtype=dtype))
+
+
+def num_threads() -> int:
+    """Threads the oracle's parallel loops use."""
+    return int(_load().sko_num_threads())
 
 
 def bf16_to_double(bits: int) -> float:

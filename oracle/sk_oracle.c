@@ -415,3 +415,16 @@ void sko_merge(const float *part_o, const float *part_m, const float *part_l,
             lse[i] = Lam > 0.0 ? M + log(Lam) : -INFINITY;
     }
 }
+
+/* Threads the OpenMP loops above use (1 without OpenMP). */
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+int sko_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

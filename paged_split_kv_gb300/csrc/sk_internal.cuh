@@ -1,0 +1,108 @@
+// Internal declarations shared by the libsk translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "sk.h"
+
+namespace sk {
+
+constexpr int kTile = 64;        // tokens per plan tile
+constexpr int kHeadDim = 128;
+constexpr int kPage = 16;
+
+// Everything the attention kernels need, resolved on the host.
+struct AttnParams {
+    const uint16_t *q;           // bf16 bits [NT, H_q, D]
+    const void *kv;              // [NB, H_kv, 16, 2D] bf16 bits or e4m3 codes
+    const int32_t *block_table;
+    const int32_t *seq_lens;
+    const int32_t *cu_q;
+    const int32_t *plan;         // NULL: fixed split
+    float *part_o, *part_m, *part_l;
+    int *status;                 // device status word
+    int64_t num_blocks;
+    int bt_stride;
+    int bs, num_tokens, max_q_len;
+    int H_q, H_kv, G;
+    int seg_max;
+    int fixed_nseg;              // segments per sequence when plan == NULL
+    int num_items;               // work items the grid covers (per KV head)
+    int causal;
+    float score_scale_log2;      // sm_scale * k_scale * log2(e)
+    float v_scale;               // applied to o (1 for bf16)
+};
+
+// A decoded work item.
+struct WorkItem {
+    int s, g;                    // sequence, segment
+    int k0, k1;                  // key range [k0, k1) of the segment (k1 <= L_s; may be empty)
+    int L, q_len, tok0;          // sequence length, query tokens, first query token
+};
+
+// Decodes work item `item` (SGLang PR 39172, Modifications: the prologue
+// reads plan[1+i], exits on -1, tiles per segment come from plan[0]).
+// Returns false when the CTA has nothing to do.
+__device__ __forceinline__ bool decode_work_item(const AttnParams &p, int item, WorkItem &w)
+{
+    int T;
+    if (p.plan != nullptr) {
+        const int code = __ldg(p.plan + 1 + item);
+        if (code < 0)
+            return false;
+        w.s = code >> 16;
+        w.g = code & 0xFFFF;
+        T = __ldg(p.plan) * kTile;
+    } else {
+        w.s = item / p.fixed_nseg;
+        w.g = item - w.s * p.fixed_nseg;
+        if (w.s >= p.bs)
+            return false;
+        const int L = __ldg(p.seq_lens + w.s);
+        const int tiles = (L + kTile - 1) / kTile;
+        int per = (tiles + p.fixed_nseg - 1) / p.fixed_nseg;
+        per = per < 1 ? 1 : per;
+        T = per * kTile;
+    }
+    if (w.s >= p.bs || w.g >= p.seg_max) {
+        atomicOr(p.status, SK_DEV_BAD_SEQ);
+        return false;
+    }
+    w.L = __ldg(p.seq_lens + w.s);
+    w.tok0 = __ldg(p.cu_q + w.s);
+    w.q_len = __ldg(p.cu_q + w.s + 1) - w.tok0;
+    const long long k0 = (long long)w.g * T;
+    long long k1 = k0 + T;
+    if (k1 > w.L)
+        k1 = w.L;
+    w.k0 = (int)(k0 < w.L ? k0 : w.L);
+    w.k1 = (int)(k1 > w.k0 ? k1 : w.k0);
+    if (w.q_len < 0 || w.q_len > p.max_q_len || w.tok0 < 0 || w.tok0 + w.q_len > p.num_tokens ||
+        w.L < 0 || (long long)w.L > (long long)p.bt_stride * kPage) {
+        atomicOr(p.status, SK_DEV_BAD_SEQ);
+        return false;
+    }
+    return true;
+}
+
+// Keys [0, n) that query token j (of q_len) of a sequence of length L sees.
+__device__ __forceinline__ int visible_keys(int L, int q_len, int j, int causal)
+{
+    if (!causal)
+        return L;
+    int n = L - q_len + j + 1;
+    n = n < L ? n : L;
+    return n > 0 ? n : 0;
+}
+
+// Launchers (each returns a cudaError_t from the launch).
+cudaError_t launch_plan(const int32_t *seq_lens, const int32_t *cu_q, int bs, int num_tokens,
+                        int budget, int seg_max, int32_t *plan, int plan_capacity,
+                        int32_t *tok_nseg, int *status, cudaStream_t stream);
+cudaError_t launch_attn_simt(const AttnParams &p, int kv_dtype, cudaStream_t stream);
+cudaError_t launch_merge(const float *part_o, const float *part_m, const float *part_l,
+                         const int32_t *tok_nseg, int fixed_nseg, int num_tokens, int H_q,
+                         int seg_max, uint16_t *out, float *lse, cudaStream_t stream);
+
+}  // namespace sk

@@ -1,0 +1,98 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, every
+function include/sk.h declares is exported, host arithmetic agrees with the
+oracle, and invalid arguments are rejected before anything touches CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def sklib():
+    from paged_split_kv_gb300 import build as b
+    b.build()
+    import paged_split_kv_gb300 as sk
+    return sk.lib()
+
+
+def _declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(sk_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(sklib):
+    names = _declared_functions()
+    assert len(names) >= 8
+    for n in names:
+        assert hasattr(sklib, n), n
+
+
+def test_tile_and_fixed_split_match_oracle(sklib, oracle):
+    assert sklib.sk_tile_tokens() == 64
+    for bs in range(1, 70):
+        for kv in (1, 2, 4, 8):
+            for nsm in (148, 152, 256):
+                for seg_max in (64, 16):
+                    assert sklib.sk_fixed_nseg(bs, kv, nsm, seg_max) == oracle.fixed_nseg(bs, kv, nsm, seg_max)
+
+
+FAKE = ctypes.c_void_p(256)   # never dereferenced: validation runs first
+
+
+def test_build_plan_rejects_bad_arguments_without_cuda(sklib):
+    f = sklib.sk_build_plan
+    # bs out of range
+    assert f(FAKE, 0, FAKE, 0, 0, 4, 2, 148, 64, FAKE, 100, FAKE, None) == -1
+    assert f(FAKE, 0, FAKE, 0, 40000, 4, 2, 148, 64, FAKE, 50000, FAKE, None) == -1
+    # null plan
+    assert f(FAKE, 0, FAKE, 0, 4, 4, 2, 148, 64, None, 100, FAKE, None) == -1
+    # capacity below 1 + max(B, bs)
+    assert f(FAKE, 0, FAKE, 0, 4, 4, 2, 148, 64, FAKE, 74, FAKE, None) == -2
+    assert b"plan_capacity" in sklib.sk_last_error()
+    # seg_max too large for the 16-bit segment field
+    assert f(FAKE, 0, FAKE, 0, 4, 4, 2, 148, 70000, FAKE, 100, FAKE, None) == -1
+
+
+def test_attention_rejects_bad_arguments_without_cuda(sklib):
+    f = sklib.sk_paged_decode_attn
+    base = dict(q=FAKE, kv=FAKE, dt=0, ks=1.0, vs=1.0, bt=FAKE, stride=10, nb=100, page=16,
+                lens=FAKE, cu=FAKE, plan=FAKE, cap=75, bs=4, nt=16, mq=4, hq=32, hkv=2, d=128,
+                scale=0.088, causal=1, nsm=148, seg=64, po=FAKE, pm=FAKE, pl=FAKE, st=None)
+
+    def call(**kw):
+        a = dict(base, **kw)
+        return f(*a.values())
+
+    assert call(d=64) == -3
+    assert call(page=32) == -3
+    assert call(hq=31) == -1
+    assert call(dt=7) == -1
+    assert call(cap=74) == -2
+    assert call(bs=0) == -1
+    assert call(q=None) == -1
+    assert call(q=ctypes.c_void_p(264)) == -1          # not 16-byte aligned
+    assert call(scale=0.0) == -1
+    assert call(dt=1, ks=0.0) == -1
+
+
+def test_merge_rejects_bad_arguments_without_cuda(sklib):
+    f = sklib.sk_merge_segments
+    assert f(FAKE, FAKE, FAKE, None, 65, 4, 8, 128, 64, FAKE, None, None) == -1
+    assert f(FAKE, FAKE, FAKE, None, 1, 4, 8, 96, 64, FAKE, None, None) == -3
+    assert f(None, FAKE, FAKE, None, 1, 4, 8, 128, 64, FAKE, None, None) == -1
+
+
+def test_python_binding_refuses_cpu_tensors(sklib):
+    import torch
+    import paged_split_kv_gb300 as sk
+    with pytest.raises(ValueError):
+        sk.sk_build_plan(torch.zeros(2, dtype=torch.int32), torch.zeros(3, dtype=torch.int32), 1,
+                         torch.zeros(10, dtype=torch.int32), torch.zeros(2, dtype=torch.int32), 148)

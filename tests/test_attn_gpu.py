@@ -1,0 +1,177 @@
+"""Attention + merge through the C ABI vs the fp64 oracle.
+
+Small problems are compared element by element (bf16 output, log-sum-exp and
+every segment partial); the five full-size workloads are compared on sampled
+rows the oracle evaluates one by one, plus invariants that hold at any size.
+Tolerances (max-abs): 1e-2 for bf16 KV, 2e-2 for fp8 KV, 8e-3 between the
+planned and the fixed split on the same inputs."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import paged_split_kv_gb300 as sk
+import sk_inputs as si
+from gpu_helpers import (TOL_PLAN_VS_FIXED, oracle_problem, oracle_sampled, problem_tensors,
+                         run_library, segments_of, tol_for, host_bits)
+from helpers import KV_BF16, KV_FP8, build_problem, repermute
+from oracle import oracle
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def _small_problems():
+    return [
+        build_problem([0, 1, 5, 17, 700, 1333, 64, 257], [4, 4, 1, 2, 4, 3, 4, 1], 32, 2, seed=21),
+        build_problem([5, 300], 1, 8, 1, seed=22),
+        build_problem([2049, 611, 0, 1], 4, 16, 2, kv_dtype=KV_FP8, k_scale=0.5, v_scale=0.25, seed=23),
+        build_problem([3, 40, 129, 1000, 2, 777, 64], [1, 3, 4, 2, 1, 4, 2], 16, 2, kv_dtype=KV_FP8,
+                      k_scale=0.5, v_scale=0.25, seed=24),
+        build_problem(list(range(1, 40)), 1, 32, 8, seed=25),
+        build_problem([50, 901], 3, 16, 2, causal=0, seed=26),
+        build_problem([4000], 4, 32, 2, seed=27),                # bs 1: long single sequence
+        build_problem([130, 70], 8, 128, 8, seed=28),            # 128 rows per work item (G16 x q8)
+        build_problem([300, 20], 2, 40, 4, seed=29),             # G = 10, rows not a power of two
+    ]
+
+
+@pytest.mark.parametrize("use_plan", [True, False])
+@pytest.mark.parametrize("k", range(9))
+def test_small_problem_elementwise(k, use_plan):
+    pr = _small_problems()[k]
+    q, kv = problem_tensors(pr, DEV)
+    r = run_library(pr, q, kv, use_plan=use_plan)
+    assert r.status == 0
+    ref, ref_lse = oracle_problem(pr)
+    got = r.out.float().cpu().numpy()
+    tol = tol_for(pr.kv_dtype)
+    assert np.isfinite(got).all()
+    err = np.max(np.abs(got - ref))
+    assert err <= tol, err
+    lse = r.lse.cpu().numpy()
+    fin = np.isfinite(ref_lse)
+    assert np.array_equal(np.isneginf(lse), ~fin)
+    assert np.max(np.abs(lse[fin] - ref_lse[fin]), initial=0) <= 1e-3
+
+
+@pytest.mark.parametrize("k", [0, 2, 3, 6])
+def test_small_problem_partials(k):
+    """Every segment partial: o / l and m + log l are the segment's unique output
+    and log-sum-exp; a row that sees no key of the segment has (-inf, 0, 0)."""
+    pr = _small_problems()[k]
+    q, kv = problem_tensors(pr, DEV)
+    for use_plan in (True, False):
+        r = run_library(pr, q, kv, use_plan=use_plan)
+        nseg, seg_tiles = segments_of(pr, use_plan)
+        po, pm, pl, _, _ = oracle.attention_split(*pr.oracle_args(), nseg, seg_tiles, 64, r.seg_max)
+        go, gm, gl = (x.cpu().numpy() for x in (r.part_o, r.part_m, r.part_l))
+        cu = pr.cu_q
+        tol = tol_for(pr.kv_dtype)
+        for s in range(pr.bs):
+            for t in range(cu[s], cu[s + 1]):
+                for g in range(int(nseg[s])):
+                    for h in range(pr.num_q_heads):
+                        if pl[t, g, h] == 0:
+                            assert gl[t, g, h] == 0 and np.isneginf(gm[t, g, h]) and not go[t, g, h].any()
+                            continue
+                        assert gl[t, g, h] > 0
+                        assert abs((gm[t, g, h] + math.log(gl[t, g, h])) - (pm[t, g, h] + math.log(pl[t, g, h]))) < 1e-3
+                        err = np.max(np.abs(go[t, g, h] / gl[t, g, h] - po[t, g, h] / pl[t, g, h]))
+                        assert err <= tol, (s, t, g, h, err)
+
+
+def test_planned_vs_fixed_split_agree():
+    for pr in _small_problems():
+        q, kv = problem_tensors(pr, DEV)
+        a = run_library(pr, q, kv, use_plan=True, num_sms=24)
+        b = run_library(pr, q, kv, use_plan=False, num_sms=24)
+        err = (a.out.float() - b.out.float()).abs().max().item()
+        assert err <= TOL_PLAN_VS_FIXED, err
+
+
+def test_block_table_permutation_is_bit_identical():
+    pr = _small_problems()[0]
+    pr2 = repermute(pr, seed=5)
+    q, kv = problem_tensors(pr, DEV)
+    q2, kv2 = problem_tensors(pr2, DEV)
+    a = run_library(pr, q, kv)
+    b = run_library(pr2, q2, kv2)
+    assert torch.equal(a.out.view(torch.int16), b.out.view(torch.int16))
+
+
+def test_v_one_gives_one_and_needle():
+    # V = 1: every row that sees a key returns exactly 1 (bf16)
+    pr = build_problem([0, 1, 5, 17, 2500], 4, 32, 2, vfun=lambda s, p, h, d: np.ones((len(p), len(d))), seed=31)
+    q, kv = problem_tensors(pr, DEV)
+    r = run_library(pr, q, kv)
+    got = r.out.float().cpu().numpy()
+    ref, _ = oracle_problem(pr)
+    seen = np.abs(ref).max(axis=-1) > 0
+    assert np.all(np.abs(got[seen] - 1.0) <= 2 ** -8)
+    assert np.all(got[~seen] == 0)
+
+    def kf(s, p, h, d):
+        k = np.zeros((len(p), len(d)))
+        k[p == 1777, :] = 40.0 / np.sqrt(128)
+        return k
+    pr = build_problem([3000], 1, 2, 1, kfun=kf, qfun=lambda t, hq, d: np.ones(len(d)), seed=32)
+    q, kv = problem_tensors(pr, DEV)
+    r = run_library(pr, q, kv)
+    want = pr.V[0][1777, 0]
+    assert np.max(np.abs(r.out.float().cpu().numpy()[0, 0] - want)) <= 1e-2
+
+
+def _run_workload(w, dev, use_plan=True):
+    q = si.make_q(w, dev)
+    kv = si.make_kv(w, dev)
+    return q, kv, run_library(w, q, kv, use_plan=use_plan)
+
+
+@pytest.mark.parametrize("idx", [1, 2, 3, 4, 5])
+def test_full_workload_sampled_rows(idx):
+    w = si.config(idx)
+    dev = torch.device(DEV)
+    q, kv, r = _run_workload(w, dev)
+    assert r.status == 0
+    out = r.out.float()
+    assert torch.isfinite(out).all()
+    rng = np.random.default_rng(1000 + idx)
+    seqs = sorted(set([int(np.argmax(w.seq_lens))] + [int(x) for x in rng.integers(0, w.bs, size=6)]))
+    samples = oracle_sampled(w, q, kv, seqs, 3, rng)
+    tol = tol_for(w.kv_dtype)
+    got = out.cpu().numpy()
+    lse = r.lse.cpu().numpy()
+    worst = 0.0
+    for t, h, o, l in samples:
+        worst = max(worst, float(np.max(np.abs(got[t, h] - o))))
+        if np.isfinite(l):
+            assert abs(lse[t, h] - l) <= 1e-3
+        else:
+            assert np.isneginf(lse[t, h])
+    assert worst <= tol, worst
+    # the planned and the fixed split agree on the same inputs
+    r2 = run_library(w, q, kv, use_plan=False)
+    diff = (r2.out.float() - out).abs().max().item()
+    assert diff <= TOL_PLAN_VS_FIXED, diff
+
+
+def test_long_sequences_with_v_one():
+    """Agentic lengths (one 248k request, 0/1/5/17-token sequences) with V = 1:
+    every row that sees a key must return exactly 1, at full length."""
+    w = si.config(3)
+    dev = torch.device(DEV)
+    q = si.make_q(w, dev)
+    kv = si.make_kv(w, dev, poison_tail=False)
+    kv[..., w.head_dim:] = 1.0
+    si.poison_unused_rows(w, kv)
+    r = run_library(w, q, kv)
+    assert r.status == 0
+    out = r.out.float().cpu().numpy()
+    for s in range(w.bs):
+        for j in range(int(w.q_lens[s])):
+            t = w.cu_q[s] + j
+            n = max(0, min(int(w.seq_lens[s]), int(w.seq_lens[s]) - int(w.q_lens[s]) + j + 1))
+            want = 1.0 if n > 0 else 0.0
+            assert np.all(np.abs(out[t] - want) <= 2 ** -8), (s, j)

@@ -1,0 +1,75 @@
+"""Plan kernel vs the oracle's plan: bit-exact T, work list (with its -1 tail)
+and per-token segment counts, on the five workloads, the small shapes and a
+random fuzz of batches."""
+import numpy as np
+import pytest
+import torch
+
+import paged_split_kv_gb300 as sk
+import sk_inputs as si
+from oracle import oracle
+
+pytestmark = pytest.mark.gpu
+
+
+def _gpu_plan(lens, q_lens, kv_heads, num_sms, seg_max, cap=None):
+    d = torch.device("cuda:0")
+    lens = np.asarray(lens, np.int32)
+    cu = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    cap = cap or sk.plan_capacity(len(lens), kv_heads, num_sms)
+    plan = torch.full((cap,), 12345, dtype=torch.int32, device=d)
+    tok = torch.full((int(cu[-1]),), 777, dtype=torch.int32, device=d)
+    sk.sk_plan_cache_reset()
+    rc = sk.sk_build_plan(torch.as_tensor(lens, device=d), torch.as_tensor(cu, device=d), kv_heads,
+                          plan, tok, num_sms, seg_max)
+    assert rc == sk.SK_OK
+    torch.cuda.synchronize()
+    assert sk.sk_get_device_status() == 0
+    return plan.cpu().numpy(), tok.cpu().numpy(), cu, cap
+
+
+def _check(lens, q_lens, kv_heads, num_sms, seg_max):
+    plan, tok, cu, cap = _gpu_plan(lens, q_lens, kv_heads, num_sms, seg_max)
+    ref, ref_tok, _, _ = oracle.plan(np.asarray(lens, np.int32), cu, kv_heads, num_sms, seg_max,
+                                     sk.sk_tile_tokens(), cap)
+    np.testing.assert_array_equal(plan, ref)
+    np.testing.assert_array_equal(tok, ref_tok)
+
+
+@pytest.mark.parametrize("idx", [1, 2, 3, 4, 5])
+def test_plan_bit_exact_on_workloads(idx):
+    w = si.config(idx)
+    _check(w.seq_lens, w.q_lens, w.num_kv_heads, w.num_sms, w.seg_max)
+
+
+def test_plan_bit_exact_on_small_shapes():
+    for w in si.small_cases():
+        _check(w.seq_lens, w.q_lens, w.num_kv_heads, w.num_sms, w.seg_max)
+
+
+def test_plan_fuzz():
+    rng = np.random.default_rng(99)
+    for trial in range(600):
+        bs = int(rng.integers(1, 400)) if trial % 50 else int(rng.integers(1000, 32768))
+        kind = trial % 4
+        if kind == 0:
+            lens = rng.integers(0, 300_000, size=bs)
+        elif kind == 1:
+            lens = np.exp(rng.uniform(0, np.log(300_000), size=bs)).astype(np.int64)
+        elif kind == 2:
+            lens = rng.integers(0, 3_000, size=bs)
+        else:
+            lens = np.zeros(bs, np.int64)
+            lens[rng.integers(0, bs)] = int(rng.integers(1, 2_000_000))
+        q = rng.integers(0, 5, size=bs)
+        kv = int(rng.choice([1, 2, 4, 8, 16]))
+        nsm = int(rng.choice([148, 152, 256, 20]))
+        seg = int(rng.choice([64, 16, 1, 300]))
+        _check(lens.astype(np.int32), q.astype(np.int32), kv, nsm, seg)
+
+
+def test_plan_capacity_above_minimum_is_padded_with_minus_one():
+    lens = np.array([5000, 70000, 3], np.int32)
+    plan, tok, cu, cap = _gpu_plan(lens, [4, 4, 4], 2, 148, 64, cap=300)
+    ref, _, _, _ = oracle.plan(lens, cu, 2, 148, 64, sk.sk_tile_tokens(), 300)
+    np.testing.assert_array_equal(plan, ref)
