@@ -34,7 +34,9 @@ def test_merge_matches_oracle(use_counts):
     torch.cuda.synchronize()
     ref, ref_lse = oracle.merge(po, pm, pl, counts if use_counts else None, fixed, nt, hq, D, seg_max)
     got = out.float().cpu().numpy().reshape(ref.shape)
-    assert np.max(np.abs(got - ref)) <= 1e-2
+    # out is bf16 rounded to nearest: within half a unit in the last place,
+    # 2^-9 of |ref| (these synthetic outputs reach |x| ~ 8, beyond a fixed 1e-2)
+    assert np.all(np.abs(got - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-6)
     gl = lse.cpu().numpy().reshape(-1)
     fin = np.isfinite(ref_lse)
     assert np.array_equal(np.isneginf(gl), ~fin)
