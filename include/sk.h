@@ -22,8 +22,9 @@
  * Conventions for every call:
  *  - Pointers marked "device" are device memory owned by the caller; the
  *    library keeps no reference after the call returns.  It allocates no
- *    device memory of its own except one status word per device (a static
- *    __device__ variable).
+ *    device memory of its own: its only device storage is one status word
+ *    per device and the fixed scratch array of
+ *    sk_paged_decode_attention_static (both static __device__ variables).
  *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
  *    legacy default stream).  No call synchronises, so the whole path can be
  *    captured into a CUDA graph.
@@ -39,6 +40,7 @@
 #ifndef SK_H_
 #define SK_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -177,6 +179,41 @@ int sk_paged_decode_attn(const void *q, const void *kv_pages, int kv_dtype, floa
 int sk_merge_segments(const float *part_o, const float *part_m, const float *part_l,
                       const int32_t *tok_nseg, int fixed_nseg, int num_tokens, int num_q_heads,
                       int head_dim, int seg_max, void *out, float *lse, void *stream);
+
+/* The whole attention call -- plan (use_plan != 0) or fixed split, split-KV
+ * attention, merge -- without any device allocation, for callers that cannot
+ * allocate: a host engine that owns all device memory through its own
+ * allocator and forbids plug-ins to call cudaMalloc, or a C caller without a
+ * caching allocator that cannot afford cudaMalloc/cudaFree (which may
+ * synchronise the device) in a serving step.  The pages have no counterpart
+ * to this call; it exists for those callers only.
+ *
+ * The caller passes inputs and outputs as for sk_build_plan,
+ * sk_paged_decode_attn and sk_merge_segments (same meanings and layouts;
+ * out bf16 [num_tokens, num_q_heads, 128], lse fp32 or NULL).  The plan,
+ * per-token segment counts and segment partials live in one file-scope
+ * device array of sk_static_scratch_bytes() = 32 MiB per GPU that loads the
+ * library, held until exit.  A call needs about
+ * num_tokens * seg_max * num_q_heads * 520 bytes plus the plan; larger calls
+ * return SK_ERR_CAPACITY and launch nothing.  The plan is rebuilt on every
+ * call (no plan cache).  All calls share the array and it keeps the last
+ * call's contents (nothing in it needs to start at zero); calls whose kernels
+ * overlap on the GPU race on it, so serialise them.  The first call on a
+ * device looks up the array's address (cudaGetSymbolAddress, once per
+ * device); make that first call before any stream capture.
+ * Returns SK_OK or a negative sk_status. */
+int sk_paged_decode_attention_static(const void *q, const void *kv_pages, int kv_dtype,
+                                     float k_scale, float v_scale, const int32_t *block_table,
+                                     int block_table_stride, int num_blocks, int page_size,
+                                     const int32_t *seq_lens, const int32_t *cu_seqlens_q,
+                                     int use_plan, int bs, int num_tokens, int max_q_len,
+                                     int num_q_heads, int num_kv_heads, int head_dim,
+                                     float sm_scale, int causal, int num_sms, int seg_max,
+                                     void *out, float *lse, void *stream);
+
+/* Size in bytes of the static scratch array used by
+ * sk_paged_decode_attention_static. */
+size_t sk_static_scratch_bytes(void);
 
 /* Synchronise `stream`, return the device status word of the current device
  * (a mask of SK_DEV_* bits, 0 when clean) and clear it when `clear` != 0.

@@ -19,7 +19,8 @@ from typing import Optional, Tuple
 __all__ = [
     "SkError", "lib", "sk_tile_tokens", "sk_fixed_nseg", "sk_build_plan", "sk_plan_cache_reset",
     "sk_plan_launch_count", "sk_paged_decode_attn", "sk_merge_segments", "sk_get_device_status",
-    "paged_decode_attention", "plan_capacity", "SK_OK", "SK_CACHED", "SK_KV_BF16", "SK_KV_FP8_E4M3",
+    "paged_decode_attention", "plan_capacity", "sk_paged_decode_attention_static",
+    "sk_static_scratch_bytes", "SK_OK", "SK_CACHED", "SK_KV_BF16", "SK_KV_FP8_E4M3",
 ]
 
 SK_OK = 0
@@ -68,6 +69,12 @@ def lib():
         L.sk_merge_segments.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, P, P, P]
         L.sk_get_device_status.restype = i32
         L.sk_get_device_status.argtypes = [P, i32]
+        L.sk_paged_decode_attention_static.restype = i32
+        L.sk_paged_decode_attention_static.argtypes = [P, P, i32, f32, f32, P, i32, i32, i32, P, P,
+                                                       i32, i32, i32, i32, i32, i32, i32, f32, i32,
+                                                       i32, i32, P, P, P]
+        L.sk_static_scratch_bytes.restype = ctypes.c_size_t
+        L.sk_static_scratch_bytes.argtypes = []
         L.sk_last_error.restype = ctypes.c_char_p
         L.sk_last_error.argtypes = []
         _lib = L
@@ -199,6 +206,36 @@ def sk_merge_segments(part_o, part_m, part_l, tok_nseg, out, lse=None, fixed_nse
                                  int(fixed_nseg), nt, hq, d, seg_max, _ptr(out), _ptr(lse),
                                  _stream(stream))
     return _check(rc, "sk_merge_segments")
+
+
+def sk_static_scratch_bytes() -> int:
+    return lib().sk_static_scratch_bytes()
+
+
+def sk_paged_decode_attention_static(q, kv_pages, block_table, seq_lens, cu_seqlens_q, out, lse=None,
+                                     *, max_q_len: int, sm_scale: float, num_sms: int,
+                                     k_scale: float = 1.0, v_scale: float = 1.0, causal: bool = True,
+                                     seg_max: int = 64, use_plan: bool = True, stream=None) -> int:
+    """The whole call without device allocation: plan, per-token counts and
+    partials live in the library's fixed 32 MiB device array.  For callers that
+    cannot allocate; calls that overlap on the GPU race on that array."""
+    import torch
+    _need(q, torch.bfloat16, "q", 3)
+    _need(kv_pages, None, "kv_pages", 4)
+    _need(block_table, torch.int32, "block_table", 2)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    _need(cu_seqlens_q, torch.int32, "cu_seqlens_q", 1)
+    _need(out, torch.bfloat16, "out", 3)
+    if lse is not None:
+        _need(lse, torch.float32, "lse", 2)
+    nt, hq, d = q.shape
+    nb, hkv, page, _ = kv_pages.shape
+    rc = lib().sk_paged_decode_attention_static(
+        _ptr(q), _ptr(kv_pages), _kv_dtype(kv_pages), float(k_scale), float(v_scale),
+        _ptr(block_table), block_table.shape[1], nb, page, _ptr(seq_lens), _ptr(cu_seqlens_q),
+        1 if use_plan else 0, seq_lens.numel(), nt, int(max_q_len), hq, hkv, d, float(sm_scale),
+        1 if causal else 0, int(num_sms), int(seg_max), _ptr(out), _ptr(lse), _stream(stream))
+    return _check(rc, "sk_paged_decode_attention_static")
 
 
 def sk_get_device_status(stream=None, clear: bool = True) -> int:

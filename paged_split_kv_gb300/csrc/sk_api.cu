@@ -91,6 +91,11 @@ std::mutex g_cache_mutex;
 std::atomic<long long> g_plan_launches{0};
 
 }  // namespace
+
+int device_status_word(int **out) { return status_ptr(out); }
+
+int set_error(int code, const char *msg) { return fail(code, "%s", msg); }
+
 }  // namespace sk
 
 using namespace sk;

@@ -96,6 +96,11 @@ __device__ __forceinline__ int visible_keys(int L, int q_len, int j, int causal)
     return n > 0 ? n : 0;
 }
 
+// Address of the current device's status word (looked up once per device).
+int device_status_word(int **out);
+// Records `msg` as this thread's last error and returns `code`.
+int set_error(int code, const char *msg);
+
 // Launchers (each returns a cudaError_t from the launch).
 cudaError_t launch_plan(const int32_t *seq_lens, const int32_t *cu_q, int bs, int num_tokens,
                         int budget, int seg_max, int32_t *plan, int plan_capacity,
