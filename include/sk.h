@@ -67,6 +67,7 @@ typedef enum {
 #define SK_DEV_BAD_BLOCK 0x1   /* a block-table entry outside [0, num_blocks) was skipped */
 #define SK_DEV_BAD_SEQ 0x2     /* q_len > max_q_len, L > block_table_stride * page, or bad cu_seqlens_q */
 #define SK_DEV_TIMEOUT 0x4     /* a bounded wait inside a kernel expired; its work item was abandoned */
+#define SK_DEV_INTERNAL 0x8    /* a kernel precondition failed (e.g. shared-memory alignment); item skipped */
 
 /* Tokens per plan tile.  The plan counts segment lengths in tiles:
  * plan[0] = tiles per segment, so a segment spans plan[0] * sk_tile_tokens()

@@ -281,7 +281,9 @@ int sk_paged_decode_attn(const void *q, const void *kv_pages, int kv_dtype, floa
     p.score_scale_log2 = sm_scale * (kv_dtype == SK_KV_FP8_E4M3 ? k_scale : 1.f) * log2e;
     p.v_scale = kv_dtype == SK_KV_FP8_E4M3 ? v_scale : 1.f;
 
-    cudaError_t e = launch_attn_simt(p, kv_dtype, static_cast<cudaStream_t>(stream));
+    const int rp = attn_tc_rows(kv_dtype, p.G * max_q_len, num_blocks, num_kv_heads);
+    cudaError_t e = rp > 0 ? launch_attn_tc(p, rp, static_cast<cudaStream_t>(stream))
+                           : launch_attn_simt(p, kv_dtype, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return cuda_fail(e, "attention kernel launch");
     return SK_OK;

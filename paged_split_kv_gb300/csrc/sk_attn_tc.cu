@@ -1,0 +1,627 @@
+// Split-KV paged attention on the tcgen05 tensor cores (bf16 pages).
+//
+// One CTA per (sequence, segment, KV head) work item, as in SGLang PR 39172
+// (Modifications, second item).  The GQA group's R = G * q_len query rows
+// (16..64) share every K/V byte, so the two products of a 128-token tile are
+// dense contractions:
+//     S^T [128 tokens x R] = K_tile [128 x 128 dims] . Q^T
+//     O^T [128 dims   x R] += V_tile^T [128 dims x 128 tokens] . P^T
+// Tokens and dimensions take the MMA's M = 128 and the query rows its N, so
+// nothing is padded for R = 16, 32 or 64.  S^T and O^T live in tensor memory
+// (TMEM lane = token for S, = dimension for O).
+//
+// Roles (192 threads):
+//   warp 0   TMA producer: for each tile, 8 pages x 4 boxes of 64 elements x
+//            16 rows (128-byte swizzle) land as [chunk][page][row][128 B], which
+//            is at once the K-major layout of K (chunks 0, 1) and the MN-major
+//            layout of V^T (chunks 2, 3).  Pages past the segment end are
+//            zero-filled (out-of-bounds box), so they cost no HBM traffic.
+//   warp 1   allocates TMEM; lane 0 issues the MMAs and commits.
+//   warps 2-5  softmax: one thread per token of the tile (its TMEM lane).
+//            The running max per query row is kept lazily: scores are
+//            exponentiated against the current max unless one beats it by
+//            2^8, and only then is the tile max reduced across the 128
+//            threads and O rescaled (which waits for the previous PV).
+//            Row sums are kept per thread and reduced once at the end.
+// Pipeline: QK(j+1) is issued before PV(j), so the tensor core works on the
+// next tile while the softmax threads handle this one; K/V stages are released
+// by the commit that follows PV.
+//
+// Every mbarrier wait is bounded (about two seconds); on expiry the CTA sets
+// SK_DEV_TIMEOUT in the device status word, waits (bounded) for its own copies
+// and MMAs in flight, frees TMEM and exits.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math_constants.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "sk_internal.cuh"
+#include "sk_sm100.cuh"
+
+namespace sk {
+namespace {
+
+using namespace sm100;
+
+constexpr int kTokTile = 128;                       // tokens per tile (MMA M)
+constexpr int kPagesPerTile = kTokTile / kPage;     // 8
+constexpr int kChunkBytes = kPage * 128;            // one page x 64 bf16 columns: 2 KB
+constexpr int kChunkRegion = kPagesPerTile * kChunkBytes;   // 16 KB: one 64-column chunk of a tile
+constexpr int kStageBytes = 4 * kChunkRegion;       // 64 KB: K lo, K hi, V lo, V hi
+constexpr int kThreads = 192;
+constexpr int kSoftmaxWarp0 = 2;
+constexpr float kRescaleLog2 = 8.0f;
+constexpr long long kWaitLimit = 4000000000LL;      // cycles (~2 s)
+constexpr uint32_t kFull = 0xffffffffu;
+constexpr int kMaxSmem = 232448;                    // 227 KB per CTA
+
+template <int RP>
+struct Cfg {
+    static_assert(RP == 16 || RP == 32 || RP == 64, "rows per work item: 16, 32 or 64");
+    static constexpr int kQBytes = 2 * RP * 128;            // two 64-column chunks of RP rows
+    static constexpr int kPBytes = kTokTile * 128;          // 128 token rows of 128 B
+    static constexpr int kMiscBytes = 2048;
+    static constexpr int kStages =
+        (3 * kStageBytes + kQBytes + kPBytes + kMiscBytes <= kMaxSmem) ? 3 : 2;
+    static constexpr int kOffQ = kStages * kStageBytes;
+    static constexpr int kOffP = kOffQ + kQBytes;
+    static constexpr int kOffMisc = kOffP + kPBytes;
+    static constexpr int kSmemBytes = kOffMisc + kMiscBytes;
+    static constexpr int kTmemCols = (3 * RP <= 64) ? 64 : (3 * RP <= 128) ? 128 : 256;
+    // misc area
+    static constexpr int kBarFull = 0;                       // [kStages]
+    static constexpr int kBarEmpty = 8 * kStages;            // [kStages]
+    static constexpr int kBarSFull = 16 * kStages;           // [2]
+    static constexpr int kBarSFree = kBarSFull + 16;         // [2]
+    static constexpr int kBarPFull = kBarSFree + 16;
+    static constexpr int kBarPFree = kBarPFull + 8;
+    static constexpr int kTmemSlot = kBarPFree + 8;
+    static constexpr int kAbort = kTmemSlot + 4;
+    static constexpr int kFlags = kAbort + 4;                // int[4]
+    static constexpr int kRed = 256;                         // float[4][RP]
+    static constexpr int kMrun = kRed + 4 * 64 * 4;          // float[RP]
+    static constexpr int kAlpha = kMrun + 64 * 4;            // float[RP]; reused for final l
+    static_assert(kAlpha + 64 * 4 <= kMiscBytes, "misc area");
+    static_assert(kSmemBytes <= kMaxSmem, "shared memory");
+    static_assert((kOffQ % 1024) == 0 && (kOffP % 1024) == 0, "1024-byte aligned operands");
+};
+
+// Sum (or max) of each of the N values across the 32 lanes of the warp.
+// Each step sends half of the live values to the partner lane `OFF` away and
+// keeps the other half, so after the steps lane l holds the result for row
+// reduce_row0<N>(l) in v[0] (N <= 32).  All indices are compile-time.
+template <int N, int OFF, bool MAX>
+struct TransposeReduce {
+    static __device__ __forceinline__ void run(float *v, int lane)
+    {
+        if constexpr (N >= 2) {
+            const bool upper = (lane & OFF) != 0;
+#pragma unroll
+            for (int i = 0; i < N / 2; ++i) {
+                const float send = upper ? v[i] : v[i + N / 2];
+                const float keep = upper ? v[i + N / 2] : v[i];
+                const float got = __shfl_xor_sync(kFull, send, OFF);
+                v[i] = MAX ? fmaxf(keep, got) : keep + got;
+            }
+            if constexpr (OFF > 1)
+                TransposeReduce<N / 2, OFF / 2, MAX>::run(v, lane);
+        } else {
+            const float got = __shfl_xor_sync(kFull, v[0], OFF);
+            v[0] = MAX ? fmaxf(v[0], got) : v[0] + got;
+            if constexpr (OFF > 1)
+                TransposeReduce<1, OFF / 2, MAX>::run(v, lane);
+        }
+    }
+};
+
+template <int N, bool MAX>
+__device__ __forceinline__ void warp_transpose_reduce(float (&v)[N], int lane)
+{
+    static_assert(N >= 1 && N <= 32, "at most one value per lane remains");
+    TransposeReduce<N, 16, MAX>::run(v, lane);
+}
+
+template <int N>
+__device__ __forceinline__ int reduce_row0(int lane)
+{
+    return lane / (32 / N);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+template <int RP>
+__global__ void __launch_bounds__(kThreads, 1)
+attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
+{
+    using C = Cfg<RP>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+
+    const int item = blockIdx.x / p.H_kv;
+    const int h = blockIdx.x - item * p.H_kv;
+    WorkItem w;
+    if (item >= p.num_items || !decode_work_item(p, item, w))
+        return;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int R = p.G * w.q_len;
+    const uint32_t sbase = smem_u32(smem);
+    if (R > RP || (sbase & 1023u) != 0) {
+        if (threadIdx.x == 0)
+            atomicOr(p.status, R > RP ? SK_DEV_BAD_SEQ : SK_DEV_INTERNAL);
+        return;
+    }
+
+    uint8_t *misc = smem + C::kOffMisc;
+    const uint32_t mbase = sbase + C::kOffMisc;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + C::kAbort);
+    volatile int *flags = reinterpret_cast<volatile int *>(misc + C::kFlags);
+    float *red = reinterpret_cast<float *>(misc + C::kRed);
+    float *m_run = reinterpret_cast<float *>(misc + C::kMrun);
+    float *alpha_s = reinterpret_cast<float *>(misc + C::kAlpha);
+    auto bar_full = [&](int s) { return mbase + C::kBarFull + 8 * s; };
+    auto bar_empty = [&](int s) { return mbase + C::kBarEmpty + 8 * s; };
+    auto bar_sfull = [&](int b) { return mbase + C::kBarSFull + 8 * b; };
+    auto bar_sfree = [&](int b) { return mbase + C::kBarSFree + 8 * b; };
+    const uint32_t bar_pfull = mbase + C::kBarPFull;
+    const uint32_t bar_pfree = mbase + C::kBarPFree;
+    const uint32_t q_s = sbase + C::kOffQ;
+    const uint32_t p_s = sbase + C::kOffP;
+    auto stage = [&](int s) { return sbase + (uint32_t)(s * kStageBytes); };
+
+    const int k0 = w.k0, k1 = w.k1;
+    const int ntiles = k1 > k0 ? (k1 - k0 + kTokTile - 1) / kTokTile : 0;
+
+    // ---- set-up: barriers, TMEM, Q in shared memory (K-major, 128-byte swizzle)
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(bar_full(s), 1);
+            mbar_init(bar_empty(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar_sfull(b), 1);
+            mbar_init(bar_sfree(b), 4);
+        }
+        mbar_init(bar_pfull, 4);
+        mbar_init(bar_pfree, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(mbase + C::kTmemSlot, C::kTmemCols);
+        tmem_relinquish();
+    }
+    for (int u = threadIdx.x; u < RP * 16; u += kThreads) {
+        const int r = u >> 4, unit = u & 15;
+        uint4 val = make_uint4(0u, 0u, 0u, 0u);
+        if (r < R) {
+            const int j = r / p.G, i = r - j * p.G;
+            const uint16_t *src = p.q + ((long long)(w.tok0 + j) * p.H_q + h * p.G + i) * kHeadDim + unit * 8;
+            val = __ldg(reinterpret_cast<const uint4 *>(src));
+        }
+        const int chunk = unit >> 3, uu = unit & 7;
+        st_shared_v4(q_s + chunk * (RP * 128) + r * 128 + ((uu ^ (r & 7)) << 4), val.x, val.y, val.z, val.w);
+    }
+    for (int r = threadIdx.x; r < RP; r += kThreads)
+        m_run[r] = -CUDART_INF_F;
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(misc + C::kTmemSlot);
+    const uint32_t tmem_s0 = tmem, tmem_o = tmem + 2 * RP;
+
+    if (warp == 0) {
+        // ================================================================ TMA producer
+        if (lane == 0)
+            prefetch_tensormap(&kv_map);
+        const int page0 = k0 / kPage;
+        const int page_end = (k1 + kPage - 1) / kPage;
+        const int32_t *bt_row = p.block_table + (long long)w.s * p.bt_stride;
+        int blk_next = -1;
+        if (lane < kPagesPerTile && page0 + lane < page_end)
+            blk_next = __ldg(bt_row + page0 + lane);
+        int issued = 0;
+        bool ok = true;
+        for (int j = 0; j < ntiles && ok; ++j) {
+            const int st = j % C::kStages;
+            if (j >= C::kStages)
+                ok = mbar_wait_bounded(bar_empty(st), ((j / C::kStages) - 1) & 1, abort_flag, kWaitLimit);
+            ok = __all_sync(kFull, ok);
+            if (!ok)
+                break;
+            const int blk = blk_next;
+            const int pg = page0 + j * kPagesPerTile + lane;
+            const int pg_next = pg + kPagesPerTile;
+            blk_next = -1;
+            if (lane < kPagesPerTile && j + 1 < ntiles && pg_next < page_end)
+                blk_next = __ldg(bt_row + pg_next);
+            if (lane == 0)
+                mbar_arrive_expect_tx(bar_full(st), kStageBytes);
+            __syncwarp();
+            if (lane < kPagesPerTile) {
+                int y = -kPage;                       // whole box out of bounds: zero fill
+                if (pg < page_end) {
+                    if (blk >= 0 && blk < p.num_blocks)
+                        y = (blk * p.H_kv + h) * kPage;
+                    else
+                        atomicOr(p.status, SK_DEV_BAD_BLOCK);
+                }
+                const uint32_t dst = stage(st) + lane * kChunkBytes;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    tma_load_2d(dst + c * kChunkRegion, &kv_map, c * 64, y, bar_full(st));
+            }
+            issued = j + 1;
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            if (lane == 0)
+                atomicOr(p.status, SK_DEV_TIMEOUT);
+            // let every copy already issued land before the CTA exits
+            for (int t = issued > C::kStages ? issued - C::kStages : 0; t < issued; ++t)
+                mbar_wait_bounded(bar_full(t % C::kStages), (t / C::kStages) & 1, nullptr, kWaitLimit);
+        }
+    } else if (warp == 1) {
+        // ================================================================ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = idesc_bf16_f32(kTokTile, RP, 0, 0);
+            constexpr uint32_t idesc_pv = idesc_bf16_f32(kTokTile, RP, 1, 1);
+            bool ok = true;
+            int last_pv = -1, last_qk = -1;
+            // step j: QK of tile j (while the softmax threads work on tile j-1), then PV of tile j-1
+            for (int j = 0; j <= ntiles && ok; ++j) {
+                if (j < ntiles) {
+                    const int st = j % C::kStages, b = j & 1;
+                    ok = mbar_wait_bounded(bar_full(st), (j / C::kStages) & 1, abort_flag, kWaitLimit);
+                    if (ok && j >= 2)
+                        ok = mbar_wait_bounded(bar_sfree(b), ((j - 2) >> 1) & 1, abort_flag, kWaitLimit);
+                    if (!ok)
+                        break;
+                    tc_fence_after();
+                    const uint32_t k_base = stage(st);
+#pragma unroll
+                    for (int k = 0; k < kHeadDim / 16; ++k) {
+                        // A = K tile: M = 128 tokens, K-major; B = Q: N = RP rows, K-major; 16 dims per step
+                        const uint32_t off = (uint32_t)((k >> 2) * kChunkRegion + (k & 3) * 32);
+                        const uint32_t qoff = (uint32_t)((k >> 2) * (RP * 128) + (k & 3) * 32);
+                        const uint64_t a = smem_desc_sw128(k_base + off, 16, 1024);
+                        const uint64_t bq = smem_desc_sw128(q_s + qoff, 16, 1024);
+                        mma_bf16_ss(tmem_s0 + b * RP, a, bq, idesc_qk, k > 0 ? 1u : 0u);
+                    }
+                    mma_commit(bar_sfull(b));
+                    last_qk = j;
+                }
+                if (j >= 1) {
+                    const int i = j - 1;
+                    ok = mbar_wait_bounded(bar_pfull, i & 1, abort_flag, kWaitLimit);
+                    if (!ok)
+                        break;
+                    tc_fence_after();
+                    const uint32_t v_base = stage(i % C::kStages) + 2 * kChunkRegion;
+#pragma unroll
+                    for (int k = 0; k < kPagesPerTile; ++k) {
+                        // A = V^T: M = 128 dims (two 64-column atoms 16 KB apart), K = the 16 tokens of page k
+                        const uint64_t a = smem_desc_sw128(v_base + k * kChunkBytes, kChunkRegion, 1024);
+                        // B = P^T: N = RP rows (one atom), K = the same 16 tokens
+                        const uint64_t bp = smem_desc_sw128(p_s + k * kChunkBytes, 1024, 1024);
+                        mma_bf16_ss(tmem_o, a, bp, idesc_pv, (i > 0 || k > 0) ? 1u : 0u);
+                    }
+                    mma_commit(bar_empty(i % C::kStages));
+                    mma_commit(bar_pfree);
+                    last_pv = i;
+                }
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                atomicOr(p.status, SK_DEV_TIMEOUT);
+                // let issued MMAs finish before TMEM is freed
+                if (last_qk >= 0)
+                    mbar_wait_bounded(bar_sfull(last_qk & 1), (last_qk >> 1) & 1, nullptr, kWaitLimit);
+                if (last_pv >= 0)
+                    mbar_wait_bounded(bar_pfree, last_pv & 1, nullptr, kWaitLimit);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ================================================================ softmax warpgroup
+        const int tw = warp - kSoftmaxWarp0;           // 0..3 within the group
+        const int quarter = warp & 3;                  // TMEM lane quarter this warp may access
+        const int tau = quarter * 32 + lane;           // token row (S) / dimension (O) of this thread
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const int tid = tw * 32 + lane;
+        const float cs = p.score_scale_log2;
+        const int causal_base = w.L - w.q_len;
+        const int last_page_end = (w.L + kPage - 1) / kPage * kPage;
+        float lsum[RP];
+#pragma unroll
+        for (int r = 0; r < RP; ++r)
+            lsum[r] = 0.f;
+        bool failed = false;
+
+        for (int j = 0; j < ntiles; ++j) {
+            const int b = j & 1;
+            float x[RP];
+            bool ok = !failed && mbar_wait_bounded(bar_sfull(b), (j >> 1) & 1, abort_flag, kWaitLimit);
+            ok = __all_sync(kFull, ok);          // tcgen05.ld is warp-collective
+            if (ok) {
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < RP; c += (RP >= 32 ? 32 : 16))
+                    tmem_ld32<(RP >= 32 ? 32 : 16)>(tmem_s0 + b * RP + c + lane_off, x + c);
+                tmem_wait_ld();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(bar_sfree(b));
+            // mask and scale: this thread's key is `tok`; row r = j' * G + i sees it when
+            // tok < segment end and (causal) j' >= tok - (L - q_len)
+            const int tok = k0 + j * kTokTile + tau;
+            const bool tok_ok = tok < k1;
+            const int ahead = tok - causal_base;       // > 0: only query tokens j' >= ahead see this key
+            const int rmin = (p.causal && ahead > 0) ? ahead * p.G : 0;
+            bool need = false;
+#pragma unroll
+            for (int r = 0; r < RP; ++r) {
+                const bool vis = ok && tok_ok && r >= rmin && r < R;
+                x[r] = vis ? x[r] * cs : -CUDART_INF_F;
+                need |= x[r] > m_run[r] + kRescaleLog2;
+            }
+            // group-wide decision: rescale needed? a wait failed?
+            const unsigned any_need = __any_sync(kFull, need);
+            const unsigned any_fail = __any_sync(kFull, !ok);
+            if (lane == 0)
+                flags[tw] = (any_need ? 1 : 0) | (any_fail ? 2 : 0);
+            named_bar_sync(1, 128);
+            const int fl = flags[0] | flags[1] | flags[2] | flags[3];
+            named_bar_sync(1, 128);
+            if (fl & 2) {
+                failed = true;
+                break;
+            }
+            if (fl & 1) {
+                // exact tile max per row across the 128 threads, 32 rows (or all 16) at a time
+                constexpr int kRc = RP >= 32 ? 32 : RP;
+#pragma unroll
+                for (int c0 = 0; c0 < RP; c0 += kRc) {
+                    float v[kRc];
+#pragma unroll
+                    for (int r = 0; r < kRc; ++r)
+                        v[r] = x[c0 + r];
+                    warp_transpose_reduce<kRc, true>(v, lane);
+                    red[tw * 64 + c0 + reduce_row0<kRc>(lane)] = v[0];
+                }
+                named_bar_sync(1, 128);
+                if (tid < RP) {
+                    const float mt = fmaxf(fmaxf(red[tid], red[64 + tid]), fmaxf(red[128 + tid], red[192 + tid]));
+                    const float mo = m_run[tid];
+                    const float mn = fmaxf(mo, mt);
+                    alpha_s[tid] = (mo == -CUDART_INF_F) ? 0.f : exp2f(mo - mn);
+                    m_run[tid] = mn;
+                }
+                named_bar_sync(1, 128);
+#pragma unroll
+                for (int r = 0; r < RP; ++r)
+                    lsum[r] *= alpha_s[r];
+                if (j > 0) {
+                    // O holds tiles < j: wait for PV(j-1), then rescale this thread's dimension
+                    bool okp = mbar_wait_bounded(bar_pfree, (j - 1) & 1, abort_flag, kWaitLimit);
+                    okp = __all_sync(kFull, okp);    // tcgen05.ld/st are warp-collective
+                    if (okp) {
+                        tc_fence_after();
+                        constexpr int kOc = RP >= 32 ? 32 : 16;
+#pragma unroll
+                        for (int c = 0; c < RP; c += kOc) {
+                            float o[kOc];
+                            tmem_ld32<kOc>(tmem_o + c + lane_off, o);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int r = 0; r < kOc; ++r)
+                                o[r] *= alpha_s[c + r];
+                            tmem_st32<kOc>(tmem_o + c + lane_off, o);
+                        }
+                        tmem_wait_st();
+                    } else {
+                        failed = true;
+                    }
+                }
+            }
+            // P buffer free?  (PV of the previous tile has read it)
+            if (j > 0 && !failed)
+                failed = !mbar_wait_bounded(bar_pfree, (j - 1) & 1, abort_flag, kWaitLimit);
+            if (!failed) {
+                // probabilities against the running max, written as this token's row of P^T:
+                // MN-major, 128-byte swizzle, 16-byte unit u of the row stored at u ^ (tau % 8)
+                const uint32_t row = p_s + (uint32_t)((tau >> 3) * 1024 + (tau & 7) * 128);
+#pragma unroll
+                for (int u = 0; u < RP / 8; ++u) {
+                    uint32_t pk[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int r = 8 * u + 2 * e;
+                        const float p0 = x[r] == -CUDART_INF_F ? 0.f : exp2f(x[r] - m_run[r]);
+                        const float p1 = x[r + 1] == -CUDART_INF_F ? 0.f : exp2f(x[r + 1] - m_run[r + 1]);
+                        lsum[r] += p0;
+                        lsum[r + 1] += p1;
+                        pk[e] = pack_bf16x2(p0, p1);
+                    }
+                    st_shared_v4(row + ((u ^ (tau & 7)) << 4), pk[0], pk[1], pk[2], pk[3]);
+                }
+                // rows past L in the sequence's last page may hold anything: zero their V
+                if (tok >= w.L && tok < last_page_end && tok < k0 + (j + 1) * kTokTile) {
+                    const uint32_t vrow = stage(j % C::kStages) + 2 * kChunkRegion + (tau >> 4) * kChunkBytes + (tau & 15) * 128;
+#pragma unroll
+                    for (int c = 0; c < 2; ++c)
+#pragma unroll
+                        for (int u = 0; u < 8; ++u)
+                            st_shared_v4(vrow + c * kChunkRegion + u * 16, 0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async_smem();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(bar_pfull);
+            if (failed) {
+                // the next tile's group decision propagates the failure
+                *abort_flag = 1;
+            }
+        }
+
+        // ---- epilogue: O complete?  then row sums across the 128 threads and the partials
+        bool okf = !failed;
+        if (okf && ntiles > 0)
+            okf = mbar_wait_bounded(bar_pfree, (ntiles - 1) & 1, abort_flag, kWaitLimit);
+        okf = __all_sync(kFull, okf);
+        {
+            const unsigned any_fail = __any_sync(kFull, !okf);
+            if (lane == 0)
+                flags[tw] = any_fail ? 2 : 0;
+        }
+        named_bar_sync(1, 128);
+        const bool write = ((flags[0] | flags[1] | flags[2] | flags[3]) & 2) == 0;
+        named_bar_sync(1, 128);
+        {
+            constexpr int kRc = RP >= 32 ? 32 : RP;
+#pragma unroll
+            for (int c0 = 0; c0 < RP; c0 += kRc) {
+                float v[kRc];
+#pragma unroll
+                for (int r = 0; r < kRc; ++r)
+                    v[r] = lsum[c0 + r];
+                warp_transpose_reduce<kRc, false>(v, lane);
+                red[tw * 64 + c0 + reduce_row0<kRc>(lane)] = v[0];
+            }
+        }
+        named_bar_sync(1, 128);
+        if (tid < RP)
+            alpha_s[tid] = (red[tid] + red[64 + tid]) + (red[128 + tid] + red[192 + tid]);
+        named_bar_sync(1, 128);
+        if (write) {
+            if (ntiles > 0)
+                tc_fence_after();
+            const long long seg_base = (long long)w.g * p.H_q + h * p.G;
+            constexpr int kOc = RP >= 32 ? 32 : 16;
+#pragma unroll
+            for (int c = 0; c < RP; c += kOc) {
+                float o[kOc];
+                if (ntiles > 0) {
+                    tmem_ld32<kOc>(tmem_o + c + lane_off, o);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int r = 0; r < kOc; ++r)
+                        o[r] = 0.f;
+                }
+#pragma unroll
+                for (int rr = 0; rr < kOc; ++rr) {
+                    const int r = c + rr;
+                    if (r < R) {
+                        const int jq = r / p.G, i = r - jq * p.G;
+                        const long long slot = (long long)(w.tok0 + jq) * p.seg_max * p.H_q + seg_base + i;
+                        const float l = alpha_s[r];
+                        p.part_o[slot * kHeadDim + tau] = l > 0.f ? o[rr] * p.v_scale : 0.f;
+                        if (tau == 0) {
+                            p.part_m[slot] = l > 0.f ? m_run[r] * 0.69314718055994531f : -CUDART_INF_F;
+                            p.part_l[slot] = l;
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    // ---- teardown: every role is done with TMEM and shared memory
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+template <int RP>
+cudaError_t launch_rp(const CUtensorMap &map, const AttnParams &p, cudaStream_t stream)
+{
+    // per device and cheap: set on every launch
+    const cudaError_t attr_err = cudaFuncSetAttribute(attn_tc_kernel<RP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                      Cfg<RP>::kSmemBytes);
+    if (attr_err != cudaSuccess)
+        return attr_err;
+    const dim3 grid((unsigned)p.num_items * (unsigned)p.H_kv);
+    attn_tc_kernel<RP><<<grid, kThreads, Cfg<RP>::kSmemBytes, stream>>>(map, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+// Rows per work item the tensor-core kernel takes (0: use the CUDA-core kernel).
+int attn_tc_rows(int kv_dtype, int rows_max, long long num_blocks, int H_kv)
+{
+    if (kv_dtype != SK_KV_BF16 || rows_max <= 8 || rows_max > 64)
+        return 0;
+    if (num_blocks * H_kv * kPage > 0x7FFFFFFFLL)
+        return 0;
+    return rows_max <= 16 ? 16 : rows_max <= 32 ? 32 : 64;
+}
+
+cudaError_t launch_attn_tc(const AttnParams &p, int rp, cudaStream_t stream)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (enc == nullptr)
+        return cudaErrorNotSupported;
+    CUtensorMap map;
+    // rows of 256 bf16 (K | V of one token of one head), one row per (block, head, token)
+    const cuuint64_t dims[2] = {(cuuint64_t)(2 * kHeadDim), (cuuint64_t)p.num_blocks * p.H_kv * kPage};
+    const cuuint64_t strides[1] = {(cuuint64_t)(2 * kHeadDim * 2)};
+    const cuuint32_t box[2] = {64, (cuuint32_t)kPage};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(p.kv), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    switch (rp) {
+    case 16:
+        return launch_rp<16>(map, p, stream);
+    case 32:
+        return launch_rp<32>(map, p, stream);
+    case 64:
+        return launch_rp<64>(map, p, stream);
+    default:
+        return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace sk
