@@ -61,13 +61,10 @@ template <int RP>
 struct Cfg {
     static_assert(RP == 16 || RP == 32 || RP == 64, "rows per work item: 16, 32 or 64");
     static constexpr int kQBytes = 2 * RP * 128;            // two 64-column chunks of RP rows
-    static constexpr int kPBytes = kTokTile * 128;          // 128 token rows of 128 B
-    static constexpr int kMiscBytes = 2048;
-    static constexpr int kStages =
-        (3 * kStageBytes + kQBytes + kPBytes + kMiscBytes <= kMaxSmem) ? 3 : 2;
+    static constexpr int kMiscBytes = 3072;
+    static constexpr int kStages = (3 * kStageBytes + kQBytes + kMiscBytes <= kMaxSmem) ? 3 : 2;
     static constexpr int kOffQ = kStages * kStageBytes;
-    static constexpr int kOffP = kOffQ + kQBytes;
-    static constexpr int kOffMisc = kOffP + kPBytes;
+    static constexpr int kOffMisc = kOffQ + kQBytes;
     static constexpr int kSmemBytes = kOffMisc + kMiscBytes;
     static constexpr int kTmemCols = (3 * RP <= 64) ? 64 : (3 * RP <= 128) ? 128 : 256;
     // misc area
@@ -77,15 +74,20 @@ struct Cfg {
     static constexpr int kBarSFree = kBarSFull + 16;         // [2]
     static constexpr int kBarPFull = kBarSFree + 16;
     static constexpr int kBarPFree = kBarPFull + 8;
-    static constexpr int kTmemSlot = kBarPFree + 8;
+    static constexpr int kBarODone = kBarPFree + 8;          // committed once, after the last PV
+    static constexpr int kTmemSlot = kBarODone + 8;
     static constexpr int kAbort = kTmemSlot + 4;
-    static constexpr int kFlags = kAbort + 4;                // int[4]
-    static constexpr int kRed = 256;                         // float[4][RP]
-    static constexpr int kMrun = kRed + 4 * 64 * 4;          // float[RP]
-    static constexpr int kAlpha = kMrun + 64 * 4;            // float[RP]; reused for final l
+    static constexpr int kFlags = kAbort + 4;                // int[3][4]: per tile parity, then the epilogue
+    static constexpr int kRed = 256;                         // float[4][64]
+    static constexpr int kMrun = kRed + 4 * 64 * 4;          // float[64] running max (log2 units)
+    static constexpr int kMthr = kMrun + 64 * 4;             // float[64] running max + rescale threshold
+    static constexpr int kMsub = kMthr + 64 * 4;             // float[64] running max with -inf -> 0
+    static constexpr int kAlpha = kMsub + 64 * 4;            // float[64]; reused for the final l
+    static_assert(kFlags + 48 <= kRed, "misc area");
     static_assert(kAlpha + 64 * 4 <= kMiscBytes, "misc area");
     static_assert(kSmemBytes <= kMaxSmem, "shared memory");
-    static_assert((kOffQ % 1024) == 0 && (kOffP % 1024) == 0, "1024-byte aligned operands");
+    static_assert((kOffQ % 1024) == 0 && (kMrun % 16) == 0 && (kMthr % 16) == 0 && (kMsub % 16) == 0,
+                  "operand and vector alignment");
 };
 
 // Sum (or max) of each of the N values across the 32 lanes of the warp.
@@ -129,6 +131,14 @@ __device__ __forceinline__ int reduce_row0(int lane)
     return lane / (32 / N);
 }
 
+// 2^x on the special-function unit, flushing subnormal results to zero; 2^-inf = 0.
+__device__ __forceinline__ float ex2_ftz(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
     uint32_t r;
@@ -168,6 +178,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
     volatile int *flags = reinterpret_cast<volatile int *>(misc + C::kFlags);
     float *red = reinterpret_cast<float *>(misc + C::kRed);
     float *m_run = reinterpret_cast<float *>(misc + C::kMrun);
+    float *m_thr = reinterpret_cast<float *>(misc + C::kMthr);
+    float *m_sub = reinterpret_cast<float *>(misc + C::kMsub);
     float *alpha_s = reinterpret_cast<float *>(misc + C::kAlpha);
     auto bar_full = [&](int s) { return mbase + C::kBarFull + 8 * s; };
     auto bar_empty = [&](int s) { return mbase + C::kBarEmpty + 8 * s; };
@@ -175,8 +187,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
     auto bar_sfree = [&](int b) { return mbase + C::kBarSFree + 8 * b; };
     const uint32_t bar_pfull = mbase + C::kBarPFull;
     const uint32_t bar_pfree = mbase + C::kBarPFree;
+    const uint32_t bar_odone = mbase + C::kBarODone;
     const uint32_t q_s = sbase + C::kOffQ;
-    const uint32_t p_s = sbase + C::kOffP;
     auto stage = [&](int s) { return sbase + (uint32_t)(s * kStageBytes); };
 
     const int k0 = w.k0, k1 = w.k1;
@@ -194,6 +206,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
         }
         mbar_init(bar_pfull, 4);
         mbar_init(bar_pfree, 1);
+        mbar_init(bar_odone, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -212,8 +225,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
         const int chunk = unit >> 3, uu = unit & 7;
         st_shared_v4(q_s + chunk * (RP * 128) + r * 128 + ((uu ^ (r & 7)) << 4), val.x, val.y, val.z, val.w);
     }
-    for (int r = threadIdx.x; r < RP; r += kThreads)
+    for (int r = threadIdx.x; r < RP; r += kThreads) {
         m_run[r] = -CUDART_INF_F;
+        m_thr[r] = -CUDART_INF_F;
+        m_sub[r] = 0.f;
+    }
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -308,13 +324,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                     if (!ok)
                         break;
                     tc_fence_after();
-                    const uint32_t v_base = stage(i % C::kStages) + 2 * kChunkRegion;
+                    const uint32_t p_base = stage(i % C::kStages);      // P^T over the tile's dead K chunk 0
+                    const uint32_t v_base = p_base + 2 * kChunkRegion;
 #pragma unroll
                     for (int k = 0; k < kPagesPerTile; ++k) {
                         // A = V^T: M = 128 dims (two 64-column atoms 16 KB apart), K = the 16 tokens of page k
                         const uint64_t a = smem_desc_sw128(v_base + k * kChunkBytes, kChunkRegion, 1024);
                         // B = P^T: N = RP rows (one atom), K = the same 16 tokens
-                        const uint64_t bp = smem_desc_sw128(p_s + k * kChunkBytes, 1024, 1024);
+                        const uint64_t bp = smem_desc_sw128(p_base + k * kChunkBytes, 1024, 1024);
                         mma_bf16_ss(tmem_o, a, bp, idesc_pv, (i > 0 || k > 0) ? 1u : 0u);
                     }
                     mma_commit(bar_empty(i % C::kStages));
@@ -322,14 +339,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                     last_pv = i;
                 }
             }
+            const bool any_mma = last_qk >= 0 || last_pv >= 0;
+            if (any_mma)
+                mma_commit(bar_odone);      // completes once every MMA issued so far has completed
             if (!ok) {
                 *abort_flag = 1;
                 atomicOr(p.status, SK_DEV_TIMEOUT);
                 // let issued MMAs finish before TMEM is freed
-                if (last_qk >= 0)
-                    mbar_wait_bounded(bar_sfull(last_qk & 1), (last_qk >> 1) & 1, nullptr, kWaitLimit);
-                if (last_pv >= 0)
-                    mbar_wait_bounded(bar_pfree, last_pv & 1, nullptr, kWaitLimit);
+                if (any_mma)
+                    mbar_wait_bounded(bar_odone, 0, nullptr, kWaitLimit);
             }
         }
         __syncwarp();
@@ -351,6 +369,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
 
         for (int j = 0; j < ntiles; ++j) {
             const int b = j & 1;
+            const int st = j % C::kStages;
             float x[RP];
             bool ok = !failed && mbar_wait_bounded(bar_sfull(b), (j >> 1) & 1, abort_flag, kWaitLimit);
             ok = __all_sync(kFull, ok);          // tcgen05.ld is warp-collective
@@ -368,24 +387,34 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             // mask and scale: this thread's key is `tok`; row r = j' * G + i sees it when
             // tok < segment end and (causal) j' >= tok - (L - q_len)
             const int tok = k0 + j * kTokTile + tau;
-            const bool tok_ok = tok < k1;
             const int ahead = tok - causal_base;       // > 0: only query tokens j' >= ahead see this key
             const int rmin = (p.causal && ahead > 0) ? ahead * p.G : 0;
             bool need = false;
+            if (ok && tok < k1 && rmin == 0 && R == RP) {
 #pragma unroll
-            for (int r = 0; r < RP; ++r) {
-                const bool vis = ok && tok_ok && r >= rmin && r < R;
-                x[r] = vis ? x[r] * cs : -CUDART_INF_F;
-                need |= x[r] > m_run[r] + kRescaleLog2;
+                for (int r = 0; r < RP; r += 4) {
+                    const float4 t = *reinterpret_cast<const float4 *>(m_thr + r);
+                    x[r] *= cs;
+                    x[r + 1] *= cs;
+                    x[r + 2] *= cs;
+                    x[r + 3] *= cs;
+                    need |= (x[r] > t.x) | (x[r + 1] > t.y) | (x[r + 2] > t.z) | (x[r + 3] > t.w);
+                }
+            } else {
+                const bool tok_vis = ok && tok < k1;
+#pragma unroll
+                for (int r = 0; r < RP; ++r) {
+                    x[r] = (tok_vis && r >= rmin && r < R) ? x[r] * cs : -CUDART_INF_F;
+                    need |= x[r] > m_thr[r];
+                }
             }
-            // group-wide decision: rescale needed? a wait failed?
+            // group-wide decision: rescale needed? a wait failed?  (flags double-buffered by tile parity)
             const unsigned any_need = __any_sync(kFull, need);
             const unsigned any_fail = __any_sync(kFull, !ok);
             if (lane == 0)
-                flags[tw] = (any_need ? 1 : 0) | (any_fail ? 2 : 0);
+                flags[4 * b + tw] = (any_need ? 1 : 0) | (any_fail ? 2 : 0);
             named_bar_sync(1, 128);
-            const int fl = flags[0] | flags[1] | flags[2] | flags[3];
-            named_bar_sync(1, 128);
+            const int fl = flags[4 * b] | flags[4 * b + 1] | flags[4 * b + 2] | flags[4 * b + 3];
             if (fl & 2) {
                 failed = true;
                 break;
@@ -409,13 +438,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                     const float mn = fmaxf(mo, mt);
                     alpha_s[tid] = (mo == -CUDART_INF_F) ? 0.f : exp2f(mo - mn);
                     m_run[tid] = mn;
+                    m_thr[tid] = mn + kRescaleLog2;
+                    m_sub[tid] = mn == -CUDART_INF_F ? 0.f : mn;
                 }
                 named_bar_sync(1, 128);
 #pragma unroll
                 for (int r = 0; r < RP; ++r)
                     lsum[r] *= alpha_s[r];
                 if (j > 0) {
-                    // O holds tiles < j: wait for PV(j-1), then rescale this thread's dimension
+                    // O holds tiles < j: wait for PV(j-1), then rescale this thread's dimension.
+                    // p_free completes once per PV; S(j) being ready means PV(j-2) is done (it was
+                    // issued before QK(j)) and PV(j) cannot start before this tile's P, so the
+                    // parity of PV(j-1) is unambiguous here.
                     bool okp = mbar_wait_bounded(bar_pfree, (j - 1) & 1, abort_flag, kWaitLimit);
                     okp = __all_sync(kFull, okp);    // tcgen05.ld/st are warp-collective
                     if (okp) {
@@ -437,35 +471,36 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                     }
                 }
             }
-            // P buffer free?  (PV of the previous tile has read it)
-            if (j > 0 && !failed)
-                failed = !mbar_wait_bounded(bar_pfree, (j - 1) & 1, abort_flag, kWaitLimit);
             if (!failed) {
-                // probabilities against the running max, written as this token's row of P^T:
-                // MN-major, 128-byte swizzle, 16-byte unit u of the row stored at u ^ (tau % 8)
-                const uint32_t row = p_s + (uint32_t)((tau >> 3) * 1024 + (tau & 7) * 128);
+                // probabilities against the running max (masked entries are -inf -> 0), written as
+                // this token's row of P^T over the tile's K chunk 0, which QK(j) no longer needs:
+                // MN-major, 128-byte swizzle, 16-byte unit u of row tau stored at u ^ (tau % 8)
+                uint8_t *prow = smem + st * kStageBytes + (tau >> 3) * 1024 + (tau & 7) * 128;
 #pragma unroll
                 for (int u = 0; u < RP / 8; ++u) {
+                    const float4 ma = *reinterpret_cast<const float4 *>(m_sub + 8 * u);
+                    const float4 mb = *reinterpret_cast<const float4 *>(m_sub + 8 * u + 4);
+                    const float mm[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
                     uint32_t pk[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int r = 8 * u + 2 * e;
-                        const float p0 = x[r] == -CUDART_INF_F ? 0.f : exp2f(x[r] - m_run[r]);
-                        const float p1 = x[r + 1] == -CUDART_INF_F ? 0.f : exp2f(x[r + 1] - m_run[r + 1]);
+                        const float p0 = ex2_ftz(x[r] - mm[2 * e]);
+                        const float p1 = ex2_ftz(x[r + 1] - mm[2 * e + 1]);
                         lsum[r] += p0;
                         lsum[r + 1] += p1;
                         pk[e] = pack_bf16x2(p0, p1);
                     }
-                    st_shared_v4(row + ((u ^ (tau & 7)) << 4), pk[0], pk[1], pk[2], pk[3]);
+                    *reinterpret_cast<uint4 *>(prow + ((u ^ (tau & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 }
                 // rows past L in the sequence's last page may hold anything: zero their V
-                if (tok >= w.L && tok < last_page_end && tok < k0 + (j + 1) * kTokTile) {
-                    const uint32_t vrow = stage(j % C::kStages) + 2 * kChunkRegion + (tau >> 4) * kChunkBytes + (tau & 15) * 128;
+                if (tok >= w.L && tok < last_page_end) {
+                    uint8_t *vrow = smem + st * kStageBytes + 2 * kChunkRegion + (tau >> 4) * kChunkBytes + (tau & 15) * 128;
 #pragma unroll
                     for (int c = 0; c < 2; ++c)
 #pragma unroll
                         for (int u = 0; u < 8; ++u)
-                            st_shared_v4(vrow + c * kChunkRegion + u * 16, 0u, 0u, 0u, 0u);
+                            *reinterpret_cast<uint4 *>(vrow + c * kChunkRegion + u * 16) = make_uint4(0u, 0u, 0u, 0u);
                 }
                 fence_proxy_async_smem();
             }
@@ -480,18 +515,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
         }
 
         // ---- epilogue: O complete?  then row sums across the 128 threads and the partials
+        // (p_free cannot tell PV(last) from PV(last-1) here: both may still be running)
         bool okf = !failed;
         if (okf && ntiles > 0)
-            okf = mbar_wait_bounded(bar_pfree, (ntiles - 1) & 1, abort_flag, kWaitLimit);
+            okf = mbar_wait_bounded(bar_odone, 0, abort_flag, kWaitLimit);
         okf = __all_sync(kFull, okf);
         {
             const unsigned any_fail = __any_sync(kFull, !okf);
             if (lane == 0)
-                flags[tw] = any_fail ? 2 : 0;
+                flags[8 + tw] = any_fail ? 2 : 0;
         }
         named_bar_sync(1, 128);
-        const bool write = ((flags[0] | flags[1] | flags[2] | flags[3]) & 2) == 0;
-        named_bar_sync(1, 128);
+        const bool write = ((flags[8] | flags[9] | flags[10] | flags[11]) & 2) == 0;
         {
             constexpr int kRc = RP >= 32 ? 32 : RP;
 #pragma unroll

@@ -175,3 +175,29 @@ def test_long_sequences_with_v_one():
             n = max(0, min(int(w.seq_lens[s]), int(w.seq_lens[s]) - int(w.q_lens[s]) + j + 1))
             want = 1.0 if n > 0 else 0.0
             assert np.all(np.abs(out[t] - want) <= 2 ** -8), (s, j)
+
+
+def test_repeated_calls_are_bit_identical_under_perturbed_timing():
+    """Every kernel orders its work through barriers, so results may not depend on
+    timing: the same call, repeated while unrelated GPU work shifts the schedule,
+    returns bit-identical outputs (a missed wait shows up here as a flaky row)."""
+    d = torch.device(DEV)
+    noise = torch.randn((2048, 2048), device=d)
+    for pr in (_small_problems()[0], _small_problems()[6], _small_problems()[8]):
+        q, kv = problem_tensors(pr, DEV)
+        ref, _ = oracle_problem(pr)
+        first = None
+        for i in range(12):
+            if i % 3 == 1:
+                noise = noise @ noise.T * 1e-3       # occupy the SMs right before the call
+            r = run_library(pr, q, kv, use_plan=(i % 2 == 0), num_sms=24 if i % 4 < 2 else 148)
+            got = r.out.view(torch.int16).clone()
+            if i < 2:
+                first = first if first is not None else {}
+                first[i % 2, i % 4 < 2] = got
+            key = (i % 2, i % 4 < 2)
+            if key in (first or {}):
+                assert torch.equal(got, first[key]), (i, key)
+            else:
+                first[key] = got
+            assert np.max(np.abs(r.out.float().cpu().numpy() - ref)) <= tol_for(pr.kv_dtype)
