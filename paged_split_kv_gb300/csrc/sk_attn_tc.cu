@@ -72,8 +72,8 @@ struct Cfg {
     static constexpr int kBarEmpty = 8 * kStages;            // [kStages]
     static constexpr int kBarSFull = 16 * kStages;           // [2]
     static constexpr int kBarSFree = kBarSFull + 16;         // [2]
-    static constexpr int kBarPFull = kBarSFree + 16;
-    static constexpr int kBarPFree = kBarPFull + 8;
+    static constexpr int kBarPFull = kBarSFree + 16;         // [2], by tile parity
+    static constexpr int kBarPFree = kBarPFull + 16;
     static constexpr int kBarODone = kBarPFree + 8;          // committed once, after the last PV
     static constexpr int kTmemSlot = kBarODone + 8;
     static constexpr int kAbort = kTmemSlot + 4;
@@ -185,7 +185,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
     auto bar_empty = [&](int s) { return mbase + C::kBarEmpty + 8 * s; };
     auto bar_sfull = [&](int b) { return mbase + C::kBarSFull + 8 * b; };
     auto bar_sfree = [&](int b) { return mbase + C::kBarSFree + 8 * b; };
-    const uint32_t bar_pfull = mbase + C::kBarPFull;
+    auto bar_pfull = [&](int b) { return mbase + C::kBarPFull + 8 * b; };
     const uint32_t bar_pfree = mbase + C::kBarPFree;
     const uint32_t bar_odone = mbase + C::kBarODone;
     const uint32_t q_s = sbase + C::kOffQ;
@@ -204,7 +204,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             mbar_init(bar_sfull(b), 1);
             mbar_init(bar_sfree(b), 4);
         }
-        mbar_init(bar_pfull, 4);
+        mbar_init(bar_pfull(0), 4);
+        mbar_init(bar_pfull(1), 4);
         mbar_init(bar_pfree, 1);
         mbar_init(bar_odone, 1);
         *abort_flag = 0;
@@ -295,34 +296,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             constexpr uint32_t idesc_pv = idesc_bf16_f32(kTokTile, RP, 1, 1);
             bool ok = true;
             int last_pv = -1, last_qk = -1;
-            // step j: QK of tile j (while the softmax threads work on tile j-1), then PV of tile j-1
-            for (int j = 0; j <= ntiles && ok; ++j) {
-                if (j < ntiles) {
-                    const int st = j % C::kStages, b = j & 1;
-                    ok = mbar_wait_bounded(bar_full(st), (j / C::kStages) & 1, abort_flag, kWaitLimit);
-                    if (ok && j >= 2)
-                        ok = mbar_wait_bounded(bar_sfree(b), ((j - 2) >> 1) & 1, abort_flag, kWaitLimit);
-                    if (!ok)
-                        break;
-                    tc_fence_after();
-                    const uint32_t k_base = stage(st);
-#pragma unroll
-                    for (int k = 0; k < kHeadDim / 16; ++k) {
-                        // A = K tile: M = 128 tokens, K-major; B = Q: N = RP rows, K-major; 16 dims per step
-                        const uint32_t off = (uint32_t)((k >> 2) * kChunkRegion + (k & 3) * 32);
-                        const uint32_t qoff = (uint32_t)((k >> 2) * (RP * 128) + (k & 3) * 32);
-                        const uint64_t a = smem_desc_sw128(k_base + off, 16, 1024);
-                        const uint64_t bq = smem_desc_sw128(q_s + qoff, 16, 1024);
-                        mma_bf16_ss(tmem_s0 + b * RP, a, bq, idesc_qk, k > 0 ? 1u : 0u);
-                    }
-                    mma_commit(bar_sfull(b));
-                    last_qk = j;
-                }
-                if (j >= 1) {
-                    const int i = j - 1;
-                    ok = mbar_wait_bounded(bar_pfull, i & 1, abort_flag, kWaitLimit);
-                    if (!ok)
-                        break;
+            // Event loop: PV(i) goes out as soon as the softmax threads have written P(i), QK(j)
+            // as soon as tile j has landed and its S buffer is free.  QK(j) also waits until
+            // PV(j-2) is issued, which keeps every barrier phase unambiguous: S(j) ready then
+            // implies PV(j-2) is done, and P_full[b] cannot run two tiles ahead of its PV.
+            long long idle_since = clock64();
+            while (last_pv + 1 < ntiles) {
+                bool progressed = false;
+                const int i = last_pv + 1;
+                if (i <= last_qk && mbar_test_wait(bar_pfull(i & 1), (i >> 1) & 1)) {
                     tc_fence_after();
                     const uint32_t p_base = stage(i % C::kStages);      // P^T over the tile's dead K chunk 0
                     const uint32_t v_base = p_base + 2 * kChunkRegion;
@@ -337,6 +319,34 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                     mma_commit(bar_empty(i % C::kStages));
                     mma_commit(bar_pfree);
                     last_pv = i;
+                    progressed = true;
+                }
+                const int j = last_qk + 1;
+                if (j < ntiles && last_pv >= j - 2) {
+                    const int st = j % C::kStages, b = j & 1;
+                    if (mbar_test_wait(bar_full(st), (j / C::kStages) & 1) &&
+                        (j < 2 || mbar_test_wait(bar_sfree(b), ((j - 2) >> 1) & 1))) {
+                        tc_fence_after();
+                        const uint32_t k_base = stage(st);
+#pragma unroll
+                        for (int k = 0; k < kHeadDim / 16; ++k) {
+                            // A = K tile: M = 128 tokens, K-major; B = Q: N = RP rows, K-major; 16 dims per step
+                            const uint32_t off = (uint32_t)((k >> 2) * kChunkRegion + (k & 3) * 32);
+                            const uint32_t qoff = (uint32_t)((k >> 2) * (RP * 128) + (k & 3) * 32);
+                            const uint64_t a = smem_desc_sw128(k_base + off, 16, 1024);
+                            const uint64_t bq = smem_desc_sw128(q_s + qoff, 16, 1024);
+                            mma_bf16_ss(tmem_s0 + b * RP, a, bq, idesc_qk, k > 0 ? 1u : 0u);
+                        }
+                        mma_commit(bar_sfull(b));
+                        last_qk = j;
+                        progressed = true;
+                    }
+                }
+                if (progressed) {
+                    idle_since = clock64();
+                } else if (*abort_flag || clock64() - idle_since > kWaitLimit) {
+                    ok = false;
+                    break;
                 }
             }
             const bool any_mma = last_qk >= 0 || last_pv >= 0;
@@ -507,7 +517,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(bar_pfull);
+                mbar_arrive(bar_pfull(b));
             if (failed) {
                 // the next tile's group decision propagates the failure
                 *abort_flag = 1;
@@ -624,7 +634,7 @@ cudaError_t launch_rp(const CUtensorMap &map, const AttnParams &p, cudaStream_t 
 // Rows per work item the tensor-core kernel takes (0: use the CUDA-core kernel).
 int attn_tc_rows(int kv_dtype, int rows_max, long long num_blocks, int H_kv)
 {
-    if (kv_dtype != SK_KV_BF16 || rows_max <= 8 || rows_max > 64)
+    if (kv_dtype != SK_KV_BF16 || rows_max < 1 || rows_max > 64)
         return 0;
     if (num_blocks * H_kv * kPage > 0x7FFFFFFFLL)
         return 0;
