@@ -282,7 +282,7 @@ int sk_paged_decode_attn(const void *q, const void *kv_pages, int kv_dtype, floa
     p.v_scale = kv_dtype == SK_KV_FP8_E4M3 ? v_scale : 1.f;
 
     const int rp = attn_tc_rows(kv_dtype, p.G * max_q_len, num_blocks, num_kv_heads);
-    cudaError_t e = rp > 0 ? launch_attn_tc(p, rp, static_cast<cudaStream_t>(stream))
+    cudaError_t e = rp > 0 ? launch_attn_tc(p, kv_dtype, rp, static_cast<cudaStream_t>(stream))
                            : launch_attn_simt(p, kv_dtype, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return cuda_fail(e, "attention kernel launch");

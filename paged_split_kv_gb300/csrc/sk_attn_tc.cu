@@ -1,31 +1,38 @@
-// Split-KV paged attention on the tcgen05 tensor cores (bf16 pages).
+// Split-KV paged attention on the tcgen05 tensor cores (bf16 or fp8-e4m3 pages).
 //
 // One CTA per (sequence, segment, KV head) work item, as in SGLang PR 39172
 // (Modifications, second item).  The GQA group's R = G * q_len query rows
-// (16..64) share every K/V byte, so the two products of a 128-token tile are
+// (up to 64) share every K/V byte, so the two products of a 128-token tile are
 // dense contractions:
 //     S^T [128 tokens x R] = K_tile [128 x 128 dims] . Q^T
 //     O^T [128 dims   x R] += V_tile^T [128 dims x 128 tokens] . P^T
-// Tokens and dimensions take the MMA's M = 128 and the query rows its N, so
-// nothing is padded for R = 16, 32 or 64.  S^T and O^T live in tensor memory
-// (TMEM lane = token for S, = dimension for O).
+// Tokens and dimensions take the MMA's M = 128 and the query rows its N
+// (16, 32 or 64 columns).  S^T and O^T live in tensor memory (TMEM lane =
+// token for S, = dimension for O).
 //
 // Roles (192 threads):
-//   warp 0   TMA producer: for each tile, 8 pages x 4 boxes of 64 elements x
-//            16 rows (128-byte swizzle) land as [chunk][page][row][128 B], which
-//            is at once the K-major layout of K (chunks 0, 1) and the MN-major
-//            layout of V^T (chunks 2, 3).  Pages past the segment end are
-//            zero-filled (out-of-bounds box), so they cost no HBM traffic.
-//   warp 1   allocates TMEM; lane 0 issues the MMAs and commits.
+//   warp 0   TMA producer (8 pages per 128-token tile, 128-byte swizzle).
+//            bf16: 4 boxes of 64 elements x 16 rows per page land as
+//            [chunk][page][row][128 B], at once the K-major layout of K
+//            (chunks 0, 1) and the MN-major layout of V^T (chunks 2, 3).
+//            fp8: 2 boxes of 128 elements x 16 rows per page: K as
+//            [page][row][128 B] (K-major, one row is all 128 dims) and V raw.
+//            Pages past the segment end are zero-filled (out-of-bounds box),
+//            so they cost no HBM traffic.
+//   warp 1   allocates TMEM; lane 0 issues the MMAs and commits, event-driven.
 //   warps 2-5  softmax: one thread per token of the tile (its TMEM lane).
 //            The running max per query row is kept lazily: scores are
 //            exponentiated against the current max unless one beats it by
 //            2^8, and only then is the tile max reduced across the 128
 //            threads and O rescaled (which waits for the previous PV).
 //            Row sums are kept per thread and reduced once at the end.
-// Pipeline: QK(j+1) is issued before PV(j), so the tensor core works on the
-// next tile while the softmax threads handle this one; K/V stages are released
-// by the commit that follows PV.
+//            P^T is written over the tile's own K area, which QK no longer
+//            needs, so every stage carries its own P buffer.
+// fp8 pages: QK runs as kind::f8f6f4 on the e4m3 K codes as they arrive, with
+// Q split into two e4m3 terms (q * 2^e_r = hi + lo, a power-of-two scale per
+// row) accumulated into the same S; each softmax thread converts its token's
+// V row to f16 (exact for e4m3) and PV runs as kind::f16 with f16 P.  The
+// scales k_scale and v_scale are folded into the score scale and the output.
 //
 // Every mbarrier wait is bounded (about two seconds); on expiry the CTA sets
 // SK_DEV_TIMEOUT in the device status word, waits (bounded) for its own copies
@@ -47,9 +54,9 @@ using namespace sm100;
 
 constexpr int kTokTile = 128;                       // tokens per tile (MMA M)
 constexpr int kPagesPerTile = kTokTile / kPage;     // 8
-constexpr int kChunkBytes = kPage * 128;            // one page x 64 bf16 columns: 2 KB
-constexpr int kChunkRegion = kPagesPerTile * kChunkBytes;   // 16 KB: one 64-column chunk of a tile
-constexpr int kStageBytes = 4 * kChunkRegion;       // 64 KB: K lo, K hi, V lo, V hi
+constexpr int kChunkBytes = kPage * 128;            // one page x 128-byte rows: 2 KB
+constexpr int kChunkRegion = kPagesPerTile * kChunkBytes;   // 16 KB: 128 token rows of 128 B
+constexpr int kStageBytes = 4 * kChunkRegion;       // 64 KB
 constexpr int kThreads = 192;
 constexpr int kSoftmaxWarp0 = 2;
 constexpr float kRescaleLog2 = 8.0f;
@@ -57,16 +64,21 @@ constexpr long long kWaitLimit = 4000000000LL;      // cycles (~2 s)
 constexpr uint32_t kFull = 0xffffffffu;
 constexpr int kMaxSmem = 232448;                    // 227 KB per CTA
 
-template <int RP>
+// Stage layout (64 KB):
+//   bf16: [0,16K) K dims 0-63 (later P^T) | [16K,32K) K dims 64-127 | [32K,48K) V dims 0-63 | [48K,64K) V dims 64-127
+//   fp8:  [0,16K) K e4m3 (later P^T)      | [16K,32K) V e4m3         | [32K,48K) V f16 dims 0-63 | [48K,64K) V f16 64-127
+template <int RP, bool FP8>
 struct Cfg {
     static_assert(RP == 16 || RP == 32 || RP == 64, "rows per work item: 16, 32 or 64");
-    static constexpr int kQBytes = 2 * RP * 128;            // two 64-column chunks of RP rows
+    static constexpr int kQBytes = 2 * RP * 128;            // bf16: two 64-column chunks; fp8: hi and lo terms
     static constexpr int kMiscBytes = 3072;
     static constexpr int kStages = (3 * kStageBytes + kQBytes + kMiscBytes <= kMaxSmem) ? 3 : 2;
     static constexpr int kOffQ = kStages * kStageBytes;
     static constexpr int kOffMisc = kOffQ + kQBytes;
     static constexpr int kSmemBytes = kOffMisc + kMiscBytes;
     static constexpr int kTmemCols = (3 * RP <= 64) ? 64 : (3 * RP <= 128) ? 128 : 256;
+    static constexpr uint32_t kTxBytes = FP8 ? 2 * kChunkRegion : 4 * kChunkRegion;   // bytes the TMA brings per stage
+    static constexpr int kOffV = 2 * kChunkRegion;           // V operand (bf16 chunks 2-3, or converted f16)
     // misc area
     static constexpr int kBarFull = 0;                       // [kStages]
     static constexpr int kBarEmpty = 8 * kStages;            // [kStages]
@@ -83,10 +95,12 @@ struct Cfg {
     static constexpr int kMthr = kMrun + 64 * 4;             // float[64] running max + rescale threshold
     static constexpr int kMsub = kMthr + 64 * 4;             // float[64] running max with -inf -> 0
     static constexpr int kAlpha = kMsub + 64 * 4;            // float[64]; reused for the final l
+    static constexpr int kCrow = kAlpha + 64 * 4;            // float[64] per-row score scale (log2 units)
     static_assert(kFlags + 48 <= kRed, "misc area");
-    static_assert(kAlpha + 64 * 4 <= kMiscBytes, "misc area");
+    static_assert(kCrow + 64 * 4 <= kMiscBytes, "misc area");
     static_assert(kSmemBytes <= kMaxSmem, "shared memory");
-    static_assert((kOffQ % 1024) == 0 && (kMrun % 16) == 0 && (kMthr % 16) == 0 && (kMsub % 16) == 0,
+    static_assert((kOffQ % 1024) == 0 && (kMrun % 16) == 0 && (kMthr % 16) == 0 && (kMsub % 16) == 0 &&
+                      (kCrow % 16) == 0,
                   "operand and vector alignment");
 };
 
@@ -139,6 +153,7 @@ __device__ __forceinline__ float ex2_ftz(float x)
     return y;
 }
 
+// Two floats to a packed pair (lo in the low half), round to nearest even.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
     uint32_t r;
@@ -146,16 +161,49 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return r;
 }
 
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Two floats to packed e4m3 codes (lo in the low byte), nearest even, saturated to +-448.
+__device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi)
+{
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Packed e4m3 pair (low 16 bits) -> packed f16 pair (exact).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v)
+{
+    uint32_t r;
+    const uint16_t h = (uint16_t)(v & 0xFFFFu);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(h));
+    return r;
+}
+
+// Low half of a packed f16 pair as float.
+__device__ __forceinline__ float f16lo_to_float(uint32_t v)
+{
+    float f;
+    const uint16_t h = (uint16_t)(v & 0xFFFFu);
+    asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"(h));
+    return f;
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
 {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
-template <int RP>
+template <int RP, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
 {
-    using C = Cfg<RP>;
+    using C = Cfg<RP, FP8>;
     extern __shared__ __align__(1024) uint8_t smem[];
 
     const int item = blockIdx.x / p.H_kv;
@@ -181,6 +229,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
     float *m_thr = reinterpret_cast<float *>(misc + C::kMthr);
     float *m_sub = reinterpret_cast<float *>(misc + C::kMsub);
     float *alpha_s = reinterpret_cast<float *>(misc + C::kAlpha);
+    float *crow = reinterpret_cast<float *>(misc + C::kCrow);
     auto bar_full = [&](int s) { return mbase + C::kBarFull + 8 * s; };
     auto bar_empty = [&](int s) { return mbase + C::kBarEmpty + 8 * s; };
     auto bar_sfull = [&](int b) { return mbase + C::kBarSFull + 8 * b; };
@@ -203,9 +252,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_sfull(b), 1);
             mbar_init(bar_sfree(b), 4);
+            mbar_init(bar_pfull(b), 4);
         }
-        mbar_init(bar_pfull(0), 4);
-        mbar_init(bar_pfull(1), 4);
         mbar_init(bar_pfree, 1);
         mbar_init(bar_odone, 1);
         *abort_flag = 0;
@@ -215,16 +263,63 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
         tmem_alloc(mbase + C::kTmemSlot, C::kTmemCols);
         tmem_relinquish();
     }
-    for (int u = threadIdx.x; u < RP * 16; u += kThreads) {
-        const int r = u >> 4, unit = u & 15;
-        uint4 val = make_uint4(0u, 0u, 0u, 0u);
-        if (r < R) {
-            const int j = r / p.G, i = r - j * p.G;
-            const uint16_t *src = p.q + ((long long)(w.tok0 + j) * p.H_q + h * p.G + i) * kHeadDim + unit * 8;
-            val = __ldg(reinterpret_cast<const uint4 *>(src));
+    if constexpr (!FP8) {
+        for (int u = threadIdx.x; u < RP * 16; u += kThreads) {
+            const int r = u >> 4, unit = u & 15;
+            uint4 val = make_uint4(0u, 0u, 0u, 0u);
+            if (r < R) {
+                const int j = r / p.G, i = r - j * p.G;
+                const uint16_t *src = p.q + ((long long)(w.tok0 + j) * p.H_q + h * p.G + i) * kHeadDim + unit * 8;
+                val = __ldg(reinterpret_cast<const uint4 *>(src));
+            }
+            const int chunk = unit >> 3, uu = unit & 7;
+            st_shared_v4(q_s + chunk * (RP * 128) + r * 128 + ((uu ^ (r & 7)) << 4), val.x, val.y, val.z, val.w);
         }
-        const int chunk = unit >> 3, uu = unit & 7;
-        st_shared_v4(q_s + chunk * (RP * 128) + r * 128 + ((uu ^ (r & 7)) << 4), val.x, val.y, val.z, val.w);
+        for (int r = threadIdx.x; r < RP; r += kThreads)
+            crow[r] = p.score_scale_log2;
+    } else {
+        // Row r of Q scaled by 2^e (max |q| lands in [128, 256)), as two e4m3 terms hi + lo.
+        // One warp per row; lane l owns dimensions 4l..4l+3.
+        for (int r = warp; r < RP; r += kThreads / 32) {
+            float qv[4] = {0.f, 0.f, 0.f, 0.f};
+            if (r < R) {
+                const int j = r / p.G, i = r - j * p.G;
+                const uint2 raw = __ldg(reinterpret_cast<const uint2 *>(
+                    p.q + ((long long)(w.tok0 + j) * p.H_q + h * p.G + i) * kHeadDim + lane * 4));
+                qv[0] = __uint_as_float(raw.x << 16);
+                qv[1] = __uint_as_float(raw.x & 0xFFFF0000u);
+                qv[2] = __uint_as_float(raw.y << 16);
+                qv[3] = __uint_as_float(raw.y & 0xFFFF0000u);
+            }
+            float amax = fmaxf(fmaxf(fabsf(qv[0]), fabsf(qv[1])), fmaxf(fabsf(qv[2]), fabsf(qv[3])));
+            for (int o = 16; o > 0; o >>= 1)
+                amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+            int e = 0;
+            if (amax > 0.f && amax < CUDART_INF_F) {
+                int ex;
+                frexpf(amax, &ex);               // amax in [2^(ex-1), 2^ex)
+                e = 8 - ex;                      // amax * 2^e in [128, 256)
+                e = e > 100 ? 100 : (e < -100 ? -100 : e);
+            }
+            float lo[4];
+            uint32_t hcodes = 0;
+#pragma unroll
+            for (int k = 0; k < 4; k += 2) {
+                const float x0 = ldexpf(qv[k], e), x1 = ldexpf(qv[k + 1], e);
+                const uint32_t hc = pack_e4m3x2(x0, x1);
+                const uint32_t hf = e4m3x2_to_f16x2(hc);              // the hi terms back, exactly
+                lo[k] = x0 - f16lo_to_float(hf);
+                lo[k + 1] = x1 - f16lo_to_float(hf >> 16);
+                hcodes |= (hc & 0xFFFFu) << (8 * k);
+            }
+            const uint32_t lcodes = (pack_e4m3x2(lo[0], lo[1]) & 0xFFFFu) | ((pack_e4m3x2(lo[2], lo[3]) & 0xFFFFu) << 16);
+            // byte offset of dims 4l..4l+3 in the swizzled 128-byte row: 16-byte unit l/4, 4 bytes at (l%4)*4
+            const uint32_t off = (uint32_t)(r * 128 + ((((lane >> 2) ^ (r & 7)) << 4) | ((lane & 3) << 2)));
+            *reinterpret_cast<uint32_t *>(smem + C::kOffQ + off) = hcodes;
+            *reinterpret_cast<uint32_t *>(smem + C::kOffQ + RP * 128 + off) = lcodes;
+            if (lane == 0)
+                crow[r] = p.score_scale_log2 * ldexpf(1.f, -e);
+        }
     }
     for (int r = threadIdx.x; r < RP; r += kThreads) {
         m_run[r] = -CUDART_INF_F;
@@ -264,7 +359,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             if (lane < kPagesPerTile && j + 1 < ntiles && pg_next < page_end)
                 blk_next = __ldg(bt_row + pg_next);
             if (lane == 0)
-                mbar_arrive_expect_tx(bar_full(st), kStageBytes);
+                mbar_arrive_expect_tx(bar_full(st), C::kTxBytes);
             __syncwarp();
             if (lane < kPagesPerTile) {
                 int y = -kPage;                       // whole box out of bounds: zero fill
@@ -275,9 +370,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                         atomicOr(p.status, SK_DEV_BAD_BLOCK);
                 }
                 const uint32_t dst = stage(st) + lane * kChunkBytes;
+                if constexpr (FP8) {
+                    tma_load_2d(dst, &kv_map, 0, y, bar_full(st));                    // K codes
+                    tma_load_2d(dst + kChunkRegion, &kv_map, 128, y, bar_full(st));   // V codes
+                } else {
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    tma_load_2d(dst + c * kChunkRegion, &kv_map, c * 64, y, bar_full(st));
+                    for (int c = 0; c < 4; ++c)
+                        tma_load_2d(dst + c * kChunkRegion, &kv_map, c * 64, y, bar_full(st));
+                }
             }
             issued = j + 1;
         }
@@ -292,8 +392,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
     } else if (warp == 1) {
         // ================================================================ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc_qk = idesc_bf16_f32(kTokTile, RP, 0, 0);
-            constexpr uint32_t idesc_pv = idesc_bf16_f32(kTokTile, RP, 1, 1);
+            // QK: bf16 kind::f16, 8 steps of 16 dims; fp8 kind::f8f6f4, 4 steps of 32 dims for each Q term.
+            // PV: V^T (MN-major, two 64-dim atoms 16 KB apart) x P^T (MN-major), 8 steps of 16 tokens.
+            constexpr uint32_t idesc_qk = FP8 ? idesc_e4m3_f32(kTokTile, RP, 0, 0) : idesc_bf16_f32(kTokTile, RP, 0, 0);
+            constexpr uint32_t idesc_pv = FP8 ? idesc_f16_f32(kTokTile, RP, 1, 1) : idesc_bf16_f32(kTokTile, RP, 1, 1);
             bool ok = true;
             int last_pv = -1, last_qk = -1;
             // Event loop: PV(i) goes out as soon as the softmax threads have written P(i), QK(j)
@@ -306,15 +408,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                 const int i = last_pv + 1;
                 if (i <= last_qk && mbar_test_wait(bar_pfull(i & 1), (i >> 1) & 1)) {
                     tc_fence_after();
-                    const uint32_t p_base = stage(i % C::kStages);      // P^T over the tile's dead K chunk 0
-                    const uint32_t v_base = p_base + 2 * kChunkRegion;
+                    const uint32_t p_base = stage(i % C::kStages);      // P^T over the tile's dead K area
+                    const uint32_t v_base = p_base + C::kOffV;
 #pragma unroll
                     for (int k = 0; k < kPagesPerTile; ++k) {
-                        // A = V^T: M = 128 dims (two 64-column atoms 16 KB apart), K = the 16 tokens of page k
                         const uint64_t a = smem_desc_sw128(v_base + k * kChunkBytes, kChunkRegion, 1024);
-                        // B = P^T: N = RP rows (one atom), K = the same 16 tokens
                         const uint64_t bp = smem_desc_sw128(p_base + k * kChunkBytes, 1024, 1024);
-                        mma_bf16_ss(tmem_o, a, bp, idesc_pv, (i > 0 || k > 0) ? 1u : 0u);
+                        mma_f16_ss(tmem_o, a, bp, idesc_pv, (i > 0 || k > 0) ? 1u : 0u);
                     }
                     mma_commit(bar_empty(i % C::kStages));
                     mma_commit(bar_pfree);
@@ -328,14 +428,24 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                         (j < 2 || mbar_test_wait(bar_sfree(b), ((j - 2) >> 1) & 1))) {
                         tc_fence_after();
                         const uint32_t k_base = stage(st);
+                        if constexpr (FP8) {
 #pragma unroll
-                        for (int k = 0; k < kHeadDim / 16; ++k) {
-                            // A = K tile: M = 128 tokens, K-major; B = Q: N = RP rows, K-major; 16 dims per step
-                            const uint32_t off = (uint32_t)((k >> 2) * kChunkRegion + (k & 3) * 32);
-                            const uint32_t qoff = (uint32_t)((k >> 2) * (RP * 128) + (k & 3) * 32);
-                            const uint64_t a = smem_desc_sw128(k_base + off, 16, 1024);
-                            const uint64_t bq = smem_desc_sw128(q_s + qoff, 16, 1024);
-                            mma_bf16_ss(tmem_s0 + b * RP, a, bq, idesc_qk, k > 0 ? 1u : 0u);
+                            for (int t = 0; t < 2; ++t)
+#pragma unroll
+                                for (int k = 0; k < 4; ++k) {
+                                    const uint64_t a = smem_desc_sw128(k_base + k * 32, 16, 1024);
+                                    const uint64_t bq = smem_desc_sw128(q_s + t * (RP * 128) + k * 32, 16, 1024);
+                                    mma_f8_ss(tmem_s0 + b * RP, a, bq, idesc_qk, (t > 0 || k > 0) ? 1u : 0u);
+                                }
+                        } else {
+#pragma unroll
+                            for (int k = 0; k < kHeadDim / 16; ++k) {
+                                const uint32_t off = (uint32_t)((k >> 2) * kChunkRegion + (k & 3) * 32);
+                                const uint32_t qoff = (uint32_t)((k >> 2) * (RP * 128) + (k & 3) * 32);
+                                const uint64_t a = smem_desc_sw128(k_base + off, 16, 1024);
+                                const uint64_t bq = smem_desc_sw128(q_s + qoff, 16, 1024);
+                                mma_f16_ss(tmem_s0 + b * RP, a, bq, idesc_qk, k > 0 ? 1u : 0u);
+                            }
                         }
                         mma_commit(bar_sfull(b));
                         last_qk = j;
@@ -368,7 +478,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
         const int tau = quarter * 32 + lane;           // token row (S) / dimension (O) of this thread
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const int tid = tw * 32 + lane;
-        const float cs = p.score_scale_log2;
         const int causal_base = w.L - w.q_len;
         const int last_page_end = (w.L + kPage - 1) / kPage * kPage;
         float lsum[RP];
@@ -400,21 +509,23 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             const int ahead = tok - causal_base;       // > 0: only query tokens j' >= ahead see this key
             const int rmin = (p.causal && ahead > 0) ? ahead * p.G : 0;
             bool need = false;
-            if (ok && tok < k1 && rmin == 0 && R == RP) {
+            // (padding rows r >= R have zero Q, so their scores are 0: harmless, and never written out)
+            if (ok && tok < k1 && rmin == 0) {
 #pragma unroll
                 for (int r = 0; r < RP; r += 4) {
                     const float4 t = *reinterpret_cast<const float4 *>(m_thr + r);
-                    x[r] *= cs;
-                    x[r + 1] *= cs;
-                    x[r + 2] *= cs;
-                    x[r + 3] *= cs;
+                    const float4 c = *reinterpret_cast<const float4 *>(crow + r);
+                    x[r] *= c.x;
+                    x[r + 1] *= c.y;
+                    x[r + 2] *= c.z;
+                    x[r + 3] *= c.w;
                     need |= (x[r] > t.x) | (x[r + 1] > t.y) | (x[r + 2] > t.z) | (x[r + 3] > t.w);
                 }
             } else {
                 const bool tok_vis = ok && tok < k1;
 #pragma unroll
                 for (int r = 0; r < RP; ++r) {
-                    x[r] = (tok_vis && r >= rmin && r < R) ? x[r] * cs : -CUDART_INF_F;
+                    x[r] = (tok_vis && r >= rmin && r < R) ? x[r] * crow[r] : -CUDART_INF_F;
                     need |= x[r] > m_thr[r];
                 }
             }
@@ -483,7 +594,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             }
             if (!failed) {
                 // probabilities against the running max (masked entries are -inf -> 0), written as
-                // this token's row of P^T over the tile's K chunk 0, which QK(j) no longer needs:
+                // this token's row of P^T over the tile's K area, which QK(j) no longer needs:
                 // MN-major, 128-byte swizzle, 16-byte unit u of row tau stored at u ^ (tau % 8)
                 uint8_t *prow = smem + st * kStageBytes + (tau >> 3) * 1024 + (tau & 7) * 128;
 #pragma unroll
@@ -499,13 +610,40 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                         const float p1 = ex2_ftz(x[r + 1] - mm[2 * e + 1]);
                         lsum[r] += p0;
                         lsum[r + 1] += p1;
-                        pk[e] = pack_bf16x2(p0, p1);
+                        pk[e] = FP8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
                     }
                     *reinterpret_cast<uint4 *>(prow + ((u ^ (tau & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 }
-                // rows past L in the sequence's last page may hold anything: zero their V
-                if (tok >= w.L && tok < last_page_end) {
-                    uint8_t *vrow = smem + st * kStageBytes + 2 * kChunkRegion + (tau >> 4) * kChunkBytes + (tau & 15) * 128;
+                const bool tail_row = tok >= w.L && tok < last_page_end;   // past L in the last page: anything
+                if constexpr (FP8) {
+                    // this token's V row: e4m3 codes (TMA-swizzled) -> f16 in the MN-major operand layout;
+                    // rows past L are written as zeros.  The codes were written by the TMA: acquire them
+                    // through the stage's barrier (its phase for this tile is complete and cannot advance
+                    // before this tile's PV has run).
+                    if (!mbar_wait_bounded(bar_full(st), (j / C::kStages) & 1, abort_flag, kWaitLimit))
+                        failed = true;
+                    const uint8_t *vraw = smem + st * kStageBytes + kChunkRegion + (tau >> 4) * kChunkBytes + (tau & 15) * 128;
+                    uint8_t *vrow = smem + st * kStageBytes + C::kOffV + (tau >> 3) * 1024 + (tau & 7) * 128;
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        uint4 cv = *reinterpret_cast<const uint4 *>(vraw + ((u ^ (tau & 7)) << 4));   // dims 16u..16u+15
+                        if (tail_row || failed)
+                            cv = make_uint4(0u, 0u, 0u, 0u);
+                        const uint32_t wv[4] = {cv.x, cv.y, cv.z, cv.w};
+                        uint32_t hv[8];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            hv[2 * k] = e4m3x2_to_f16x2(wv[k]);
+                            hv[2 * k + 1] = e4m3x2_to_f16x2(wv[k] >> 16);
+                        }
+                        // f16 dims 16u..16u+7 and 16u+8..16u+15: atom (16u)/64, units 2(u%4) and 2(u%4)+1
+                        uint8_t *atom = vrow + (u >> 2) * kChunkRegion;
+                        const int u0 = 2 * (u & 3);
+                        *reinterpret_cast<uint4 *>(atom + ((u0 ^ (tau & 7)) << 4)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+                        *reinterpret_cast<uint4 *>(atom + (((u0 + 1) ^ (tau & 7)) << 4)) = make_uint4(hv[4], hv[5], hv[6], hv[7]);
+                    }
+                } else if (tail_row) {
+                    uint8_t *vrow = smem + st * kStageBytes + C::kOffV + (tau >> 4) * kChunkBytes + (tau & 15) * 128;
 #pragma unroll
                     for (int c = 0; c < 2; ++c)
 #pragma unroll
@@ -616,16 +754,17 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-template <int RP>
+template <int RP, bool FP8>
 cudaError_t launch_rp(const CUtensorMap &map, const AttnParams &p, cudaStream_t stream)
 {
     // per device and cheap: set on every launch
-    const cudaError_t attr_err = cudaFuncSetAttribute(attn_tc_kernel<RP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                      Cfg<RP>::kSmemBytes);
+    const cudaError_t attr_err = cudaFuncSetAttribute(attn_tc_kernel<RP, FP8>,
+                                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                      Cfg<RP, FP8>::kSmemBytes);
     if (attr_err != cudaSuccess)
         return attr_err;
     const dim3 grid((unsigned)p.num_items * (unsigned)p.H_kv);
-    attn_tc_kernel<RP><<<grid, kThreads, Cfg<RP>::kSmemBytes, stream>>>(map, p);
+    attn_tc_kernel<RP, FP8><<<grid, kThreads, Cfg<RP, FP8>::kSmemBytes, stream>>>(map, p);
     return cudaGetLastError();
 }
 
@@ -634,36 +773,43 @@ cudaError_t launch_rp(const CUtensorMap &map, const AttnParams &p, cudaStream_t 
 // Rows per work item the tensor-core kernel takes (0: use the CUDA-core kernel).
 int attn_tc_rows(int kv_dtype, int rows_max, long long num_blocks, int H_kv)
 {
-    if (kv_dtype != SK_KV_BF16 || rows_max < 1 || rows_max > 64)
+    if ((kv_dtype != SK_KV_BF16 && kv_dtype != SK_KV_FP8_E4M3) || rows_max < 1 || rows_max > 64)
         return 0;
     if (num_blocks * H_kv * kPage > 0x7FFFFFFFLL)
         return 0;
     return rows_max <= 16 ? 16 : rows_max <= 32 ? 32 : 64;
 }
 
-cudaError_t launch_attn_tc(const AttnParams &p, int rp, cudaStream_t stream)
+cudaError_t launch_attn_tc(const AttnParams &p, int kv_dtype, int rp, cudaStream_t stream)
 {
     EncodeTiledFn enc = encode_fn();
     if (enc == nullptr)
         return cudaErrorNotSupported;
+    const bool fp8 = kv_dtype == SK_KV_FP8_E4M3;
     CUtensorMap map;
-    // rows of 256 bf16 (K | V of one token of one head), one row per (block, head, token)
+    // one row of 2 * 128 elements (K | V of one token of one head) per (block, head, token)
     const cuuint64_t dims[2] = {(cuuint64_t)(2 * kHeadDim), (cuuint64_t)p.num_blocks * p.H_kv * kPage};
-    const cuuint64_t strides[1] = {(cuuint64_t)(2 * kHeadDim * 2)};
-    const cuuint32_t box[2] = {64, (cuuint32_t)kPage};
+    const cuuint64_t strides[1] = {(cuuint64_t)(2 * kHeadDim * (fp8 ? 1 : 2))};
+    const cuuint32_t box[2] = {fp8 ? 128u : 64u, (cuuint32_t)kPage};     // 128-byte box rows
     const cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(p.kv), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = enc(&map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                     const_cast<void *>(p.kv), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
-    switch (rp) {
-    case 16:
-        return launch_rp<16>(map, p, stream);
+    switch (rp * 2 + (fp8 ? 1 : 0)) {
     case 32:
-        return launch_rp<32>(map, p, stream);
+        return launch_rp<16, false>(map, p, stream);
     case 64:
-        return launch_rp<64>(map, p, stream);
+        return launch_rp<32, false>(map, p, stream);
+    case 128:
+        return launch_rp<64, false>(map, p, stream);
+    case 33:
+        return launch_rp<16, true>(map, p, stream);
+    case 65:
+        return launch_rp<32, true>(map, p, stream);
+    case 129:
+        return launch_rp<64, true>(map, p, stream);
     default:
         return cudaErrorInvalidValue;
     }
