@@ -50,11 +50,12 @@ def _args():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="sk", choices=["sk", "reference"])
-    ap.add_argument("--config", type=int, default=2, help="workload 1..5 (default 2)")
+    ap.add_argument("--config", type=int, default=2, help="workload 1..7 (default 2)")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--fixed-split", action="store_true", help="time the fixed split instead of the plan")
+    ap.add_argument("--fixed-split", action="store_true",
+                    help="time the fixed split even when bs > 1 (bs == 1 always uses it, as the method does)")
     return ap.parse_args()
 
 
@@ -63,6 +64,22 @@ def _dist():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return ws, rank, local
+
+
+def max_over_ranks(value: float, world_size: int, device=None) -> float:
+    """Largest `value` over all ranks (the slowest rank sets the job time)."""
+    if world_size == 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_tbps(bytes_per_rank_per_step: int, steps: int, world_size: int, max_ms: float) -> float:
+    """Whole-job throughput: every rank processed its own batch each step."""
+    return world_size * bytes_per_rank_per_step * steps / (max_ms * 1e-3) / 1e12
 
 
 def _config_json(w, extra=None):
@@ -245,11 +262,16 @@ def _peaks():
     return FALLBACK_HBM_GBS, "of fallback"
 
 
+ATTN_SOURCES = ("sk_attn_tc.cu", "sk_sm100.cuh", "sk_internal.cuh")
+
+
 def _kernel_sources_sha():
+    """Short hash of the attention kernel's sources: an ncu traffic figure is
+    only reported while it was taken on exactly these sources."""
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "paged_split_kv_gb300", "csrc", "*"))):
-        with open(f, "rb") as fh:
-            h.update(os.path.basename(f).encode())
+    for name in ATTN_SOURCES:
+        with open(os.path.join(ROOT, "paged_split_kv_gb300", "csrc", name), "rb") as fh:
+            h.update(name.encode())
             h.update(fh.read())
     return h.hexdigest()[:16]
 
@@ -289,7 +311,7 @@ def run_sk(a, w, ws, rank, local):
     bt = torch.as_tensor(w.block_table, device=dev)
     lens = torch.as_tensor(w.seq_lens, device=dev)
     cu = torch.as_tensor(w.cu_q, device=dev)
-    use_plan = not a.fixed_split
+    use_plan = w.bs > 1 and not a.fixed_split
     nsm = w.num_sms
     hkv = w.num_kv_heads
     nt = w.num_tokens
@@ -347,13 +369,9 @@ def run_sk(a, w, ws, rank, local):
     plan_ms = [e[0].elapsed_time(e[1]) for e in evs]
     attn_ms = [e[1].elapsed_time(e[2]) for e in evs]
     merge_ms = [e[2].elapsed_time(e[3]) for e in evs]
-    total_ms = evs[0][0].elapsed_time(evs[-1][3])
-    if ws > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(evs[0][0].elapsed_time(evs[-1][3]), ws, dev)
     ms_per_step = total_ms / a.steps
-    value = ws * w.kv_bytes * a.steps / (total_ms * 1e-3) / 1e12
+    value = weak_scaling_tbps(w.kv_bytes, a.steps, ws, total_ms)
 
     # end to end through the public call with host inputs (pinned), copies inside the region
     e2e = None
@@ -393,13 +411,9 @@ def run_sk(a, w, ws, rank, local):
             e2e_step()
         e1.record()
         torch.cuda.synchronize()
-        e2e_ms = e0.elapsed_time(e1)
-        if ws > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), ws, dev)
         assert torch.equal(out_h, out.cpu()), "end-to-end output differs from the device-resident run"
-        e2e = {"value": ws * w.kv_bytes * a.e2e_steps / (e2e_ms * 1e-3) / 1e12, "unit": "TB/s",
+        e2e = {"value": weak_scaling_tbps(w.kv_bytes, a.e2e_steps, ws, e2e_ms), "unit": "TB/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": e2e_ms / a.e2e_steps}
         del host, dq, dkv

@@ -177,6 +177,8 @@ def config(index: int) -> Workload:
     4 draft-extend     bs 20, same fixed five + 15 log-uniform, total 2,320,000, q ~ U{1..4},
                        16/2 heads, fp8 e4m3 KV (k_scale 0.5, v_scale 0.25)
     5 high-batch       bs 128 x 8192, q 1, 32/8 heads, bf16
+    6 bs1 long         bs 1 x 110000, q 4, 32/2 heads, bf16 (the fixed-split bypass)
+    7 bs1 longest      bs 1 x 248000, q 4, 32/2 heads, bf16 (the fixed-split bypass)
     """
     seed = 1000 + index
     rng = np.random.default_rng(seed)
@@ -194,6 +196,10 @@ def config(index: int) -> Workload:
                              kv_dtype=KV_FP8, k_scale=0.5, v_scale=0.25, rng=rng)
     if index == 5:
         return make_workload("high_batch_decode_128x8192", [8192] * 128, 1, 32, 8, seed, rng=rng)
+    if index == 6:
+        return make_workload("bs1_long_110k_q4", [110000], 4, 32, 2, seed, rng=rng)
+    if index == 7:
+        return make_workload("bs1_long_248k_q4", [248000], 4, 32, 2, seed, rng=rng)
     raise ValueError(f"no workload {index}")
 
 
