@@ -10,7 +10,7 @@
 // (16, 32 or 64 columns).  S^T and O^T live in tensor memory (TMEM lane =
 // token for S, = dimension for O).
 //
-// Roles (192 threads):
+// Roles (352 threads):
 //   warp 0   TMA producer (8 pages per 128-token tile, 128-byte swizzle).
 //            bf16: 4 boxes of 64 elements x 16 rows per page land as
 //            [chunk][page][row][128 B], at once the K-major layout of K
@@ -19,8 +19,12 @@
 //            [page][row][128 B] (K-major, one row is all 128 dims) and V raw.
 //            Pages past the segment end are zero-filled (out-of-bounds box),
 //            so they cost no HBM traffic.
-//   warp 1   allocates TMEM; lane 0 issues the MMAs and commits, event-driven.
-//   warps 2-5  softmax: one thread per token of the tile (its TMEM lane).
+//   warp 1   allocates TMEM; lane 0 issues the QK products.
+//   warp 10  lane 0 issues the PV products (one issuing thread could not keep
+//            up: a tcgen05.mma costs its issuer ~80 cycles).
+//   warps 2-9  softmax, two warpgroups: one thread per token of the tile (its
+//            TMEM lane); warps 2-5 take the first half of the query rows,
+//            warps 6-9 the second, each group on its own.
 //            The running max per query row is kept lazily: scores are
 //            exponentiated against the current max unless one beats it by
 //            2^8, and only then is the tile max reduced across the 128
@@ -57,8 +61,11 @@ constexpr int kPagesPerTile = kTokTile / kPage;     // 8
 constexpr int kChunkBytes = kPage * 128;            // one page x 128-byte rows: 2 KB
 constexpr int kChunkRegion = kPagesPerTile * kChunkBytes;   // 16 KB: 128 token rows of 128 B
 constexpr int kStageBytes = 4 * kChunkRegion;       // 64 KB
-constexpr int kThreads = 192;
 constexpr int kSoftmaxWarp0 = 2;
+constexpr int kSoftmaxGroups = 2;                   // warpgroups splitting the query rows
+constexpr int kSoftmaxWarps = 4 * kSoftmaxGroups;
+constexpr int kPvWarp = kSoftmaxWarp0 + kSoftmaxWarps;   // 10: issues the PV products
+constexpr int kThreads = 32 * (kPvWarp + 1);        // 352
 constexpr float kRescaleLog2 = 8.0f;
 constexpr long long kWaitLimit = 4000000000LL;      // cycles (~2 s)
 constexpr uint32_t kFull = 0xffffffffu;
@@ -71,8 +78,10 @@ template <int RP, bool FP8>
 struct Cfg {
     static_assert(RP == 16 || RP == 32 || RP == 64, "rows per work item: 16, 32 or 64");
     static constexpr int kQBytes = 2 * RP * 128;            // bf16: two 64-column chunks; fp8: hi and lo terms
-    static constexpr int kMiscBytes = 3072;
+    static constexpr int kMiscBytes = 4096;
+    static constexpr int kRH = RP / kSoftmaxGroups;          // rows per softmax warpgroup
     static constexpr int kStages = (3 * kStageBytes + kQBytes + kMiscBytes <= kMaxSmem) ? 3 : 2;
+    static_assert(kStages <= 3, "p_free phases rely on PV(j - 3) being done once tile j has landed");
     static constexpr int kOffQ = kStages * kStageBytes;
     static constexpr int kOffMisc = kOffQ + kQBytes;
     static constexpr int kSmemBytes = kOffMisc + kMiscBytes;
@@ -85,18 +94,19 @@ struct Cfg {
     static constexpr int kBarSFull = 16 * kStages;           // [2]
     static constexpr int kBarSFree = kBarSFull + 16;         // [2]
     static constexpr int kBarPFull = kBarSFree + 16;         // [2], by tile parity
-    static constexpr int kBarPFree = kBarPFull + 16;
-    static constexpr int kBarODone = kBarPFree + 8;          // committed once, after the last PV
+    static constexpr int kBarPFree = kBarPFull + 16;         // [2], by tile parity
+    static constexpr int kBarODone = kBarPFree + 16;         // committed once, after the last PV
     static constexpr int kTmemSlot = kBarODone + 8;
     static constexpr int kAbort = kTmemSlot + 4;
-    static constexpr int kFlags = kAbort + 4;                // int[3][4]: per tile parity, then the epilogue
-    static constexpr int kRed = 256;                         // float[4][64]
-    static constexpr int kMrun = kRed + 4 * 64 * 4;          // float[64] running max (log2 units)
+    static constexpr int kPvIssued = kAbort + 4;             // int: PVs issued so far (written by the PV thread)
+    static constexpr int kFlags = kPvIssued + 4;             // int[group][3][4]: per tile parity, then the epilogue
+    static constexpr int kRed = 256;                         // float[group][4][32]
+    static constexpr int kMrun = kRed + kSoftmaxGroups * 4 * 32 * 4;   // float[64] running max (log2 units)
     static constexpr int kMthr = kMrun + 64 * 4;             // float[64] running max + rescale threshold
     static constexpr int kMsub = kMthr + 64 * 4;             // float[64] running max with -inf -> 0
     static constexpr int kAlpha = kMsub + 64 * 4;            // float[64]; reused for the final l
     static constexpr int kCrow = kAlpha + 64 * 4;            // float[64] per-row score scale (log2 units)
-    static_assert(kFlags + 48 <= kRed, "misc area");
+    static_assert(kFlags + kSoftmaxGroups * 48 <= kRed, "misc area");
     static_assert(kCrow + 64 * 4 <= kMiscBytes, "misc area");
     static_assert(kSmemBytes <= kMaxSmem, "shared memory");
     static_assert((kOffQ % 1024) == 0 && (kMrun % 16) == 0 && (kMthr % 16) == 0 && (kMsub % 16) == 0 &&
@@ -235,7 +245,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
     auto bar_sfull = [&](int b) { return mbase + C::kBarSFull + 8 * b; };
     auto bar_sfree = [&](int b) { return mbase + C::kBarSFree + 8 * b; };
     auto bar_pfull = [&](int b) { return mbase + C::kBarPFull + 8 * b; };
-    const uint32_t bar_pfree = mbase + C::kBarPFree;
+    auto bar_pfree = [&](int b) { return mbase + C::kBarPFree + 8 * b; };
+    volatile int *pv_issued = reinterpret_cast<volatile int *>(misc + C::kPvIssued);
     const uint32_t bar_odone = mbase + C::kBarODone;
     const uint32_t q_s = sbase + C::kOffQ;
     auto stage = [&](int s) { return sbase + (uint32_t)(s * kStageBytes); };
@@ -251,12 +262,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_sfull(b), 1);
-            mbar_init(bar_sfree(b), 4);
-            mbar_init(bar_pfull(b), 4);
+            mbar_init(bar_sfree(b), kSoftmaxWarps);
+            mbar_init(bar_pfull(b), kSoftmaxWarps);
         }
-        mbar_init(bar_pfree, 1);
+        mbar_init(bar_pfree(0), 1);
+        mbar_init(bar_pfree(1), 1);
         mbar_init(bar_odone, 1);
         *abort_flag = 0;
+        *pv_issued = 0;
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -389,114 +402,167 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             for (int t = issued > C::kStages ? issued - C::kStages : 0; t < issued; ++t)
                 mbar_wait_bounded(bar_full(t % C::kStages), (t / C::kStages) & 1, nullptr, kWaitLimit);
         }
-    } else if (warp == 1) {
-        // ================================================================ MMA issuer
+    } else if (warp == 1 || warp == kPvWarp) {
+        // ================================================================ MMA issuers
+        // QK: bf16 kind::f16, 8 steps of 16 dims; fp8 kind::f8f6f4, 4 steps of 32 dims per Q term.
+        // PV: V^T (MN-major, two 64-dim atoms 16 KB apart) x P^T (MN-major), 8 steps of 16 tokens.
+        // Descriptors are built once for stage 0 / Q; an operand elsewhere is the same descriptor
+        // advanced by (byte offset >> 4) in its start-address field (shared addresses < 256 KB).
         if (lane == 0) {
-            // QK: bf16 kind::f16, 8 steps of 16 dims; fp8 kind::f8f6f4, 4 steps of 32 dims for each Q term.
-            // PV: V^T (MN-major, two 64-dim atoms 16 KB apart) x P^T (MN-major), 8 steps of 16 tokens.
             constexpr uint32_t idesc_qk = FP8 ? idesc_e4m3_f32(kTokTile, RP, 0, 0) : idesc_bf16_f32(kTokTile, RP, 0, 0);
             constexpr uint32_t idesc_pv = FP8 ? idesc_f16_f32(kTokTile, RP, 1, 1) : idesc_bf16_f32(kTokTile, RP, 1, 1);
+            const uint64_t d_kv0 = smem_desc_sw128(stage(0), 16, 1024);                    // K-major K tile
+            const uint64_t d_v0 = smem_desc_sw128(stage(0) + C::kOffV, kChunkRegion, 1024);  // MN-major V^T
+            const uint64_t d_p0 = smem_desc_sw128(stage(0), 1024, 1024);                   // MN-major P^T
+            const uint64_t d_q0 = smem_desc_sw128(q_s, 16, 1024);                          // K-major Q
+            auto adv = [](uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); };
             bool ok = true;
-            int last_pv = -1, last_qk = -1;
-            // Event loop: PV(i) goes out as soon as the softmax threads have written P(i), QK(j)
-            // as soon as tile j has landed and its S buffer is free.  QK(j) also waits until
-            // PV(j-2) is issued, which keeps every barrier phase unambiguous: S(j) ready then
-            // implies PV(j-2) is done, and P_full[b] cannot run two tiles ahead of its PV.
-            long long idle_since = clock64();
-            while (last_pv + 1 < ntiles) {
-                bool progressed = false;
-                const int i = last_pv + 1;
-                if (i <= last_qk && mbar_test_wait(bar_pfull(i & 1), (i >> 1) & 1)) {
-                    tc_fence_after();
-                    const uint32_t p_base = stage(i % C::kStages);      // P^T over the tile's dead K area
-                    const uint32_t v_base = p_base + C::kOffV;
-#pragma unroll
-                    for (int k = 0; k < kPagesPerTile; ++k) {
-                        const uint64_t a = smem_desc_sw128(v_base + k * kChunkBytes, kChunkRegion, 1024);
-                        const uint64_t bp = smem_desc_sw128(p_base + k * kChunkBytes, 1024, 1024);
-                        mma_f16_ss(tmem_o, a, bp, idesc_pv, (i > 0 || k > 0) ? 1u : 0u);
-                    }
-                    mma_commit(bar_empty(i % C::kStages));
-                    mma_commit(bar_pfree);
-                    last_pv = i;
-                    progressed = true;
-                }
-                const int j = last_qk + 1;
-                if (j < ntiles && last_pv >= j - 2) {
+            int last = -1;
+            if (warp == 1) {
+                // QK(j) once tile j has landed, its S buffer is free, and PV(j-2) is issued.  The last
+                // condition keeps barrier phases unambiguous: P_full[b] cannot run two tiles ahead of
+                // its PV, and the softmax never runs more than one tile ahead of the PVs it waits on.
+                for (int j = 0; j < ntiles && ok; ++j) {
                     const int st = j % C::kStages, b = j & 1;
-                    if (mbar_test_wait(bar_full(st), (j / C::kStages) & 1) &&
-                        (j < 2 || mbar_test_wait(bar_sfree(b), ((j - 2) >> 1) & 1))) {
-                        tc_fence_after();
-                        const uint32_t k_base = stage(st);
-                        if constexpr (FP8) {
-#pragma unroll
-                            for (int t = 0; t < 2; ++t)
-#pragma unroll
-                                for (int k = 0; k < 4; ++k) {
-                                    const uint64_t a = smem_desc_sw128(k_base + k * 32, 16, 1024);
-                                    const uint64_t bq = smem_desc_sw128(q_s + t * (RP * 128) + k * 32, 16, 1024);
-                                    mma_f8_ss(tmem_s0 + b * RP, a, bq, idesc_qk, (t > 0 || k > 0) ? 1u : 0u);
-                                }
-                        } else {
-#pragma unroll
-                            for (int k = 0; k < kHeadDim / 16; ++k) {
-                                const uint32_t off = (uint32_t)((k >> 2) * kChunkRegion + (k & 3) * 32);
-                                const uint32_t qoff = (uint32_t)((k >> 2) * (RP * 128) + (k & 3) * 32);
-                                const uint64_t a = smem_desc_sw128(k_base + off, 16, 1024);
-                                const uint64_t bq = smem_desc_sw128(q_s + qoff, 16, 1024);
-                                mma_f16_ss(tmem_s0 + b * RP, a, bq, idesc_qk, k > 0 ? 1u : 0u);
+                    ok = mbar_wait_bounded(bar_full(st), (j / C::kStages) & 1, abort_flag, kWaitLimit);
+                    if (ok && j >= 2)
+                        ok = mbar_wait_bounded(bar_sfree(b), ((j - 2) >> 1) & 1, abort_flag, kWaitLimit);
+                    if (ok && *pv_issued < j - 1) {
+                        const long long t0 = clock64();
+                        while (*pv_issued < j - 1) {
+                            if (*abort_flag || clock64() - t0 > kWaitLimit) {
+                                ok = false;
+                                break;
                             }
                         }
-                        mma_commit(bar_sfull(b));
-                        last_qk = j;
-                        progressed = true;
                     }
+                    if (!ok)
+                        break;
+                    tc_fence_after();
+                    const uint32_t so = (uint32_t)(st * kStageBytes);
+                    if constexpr (FP8) {
+#pragma unroll
+                        for (int t = 0; t < 2; ++t)
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                mma_f8_ss(tmem_s0 + b * RP, adv(d_kv0, so + k * 32), adv(d_q0, t * (RP * 128) + k * 32),
+                                          idesc_qk, (t > 0 || k > 0) ? 1u : 0u);
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < kHeadDim / 16; ++k) {
+                            const uint32_t off = (uint32_t)((k >> 2) * kChunkRegion + (k & 3) * 32);
+                            const uint32_t qoff = (uint32_t)((k >> 2) * (RP * 128) + (k & 3) * 32);
+                            mma_f16_ss(tmem_s0 + b * RP, adv(d_kv0, so + off), adv(d_q0, qoff), idesc_qk, k > 0 ? 1u : 0u);
+                        }
+                    }
+                    mma_commit(bar_sfull(b));
+                    last = j;
                 }
-                if (progressed) {
-                    idle_since = clock64();
-                } else if (*abort_flag || clock64() - idle_since > kWaitLimit) {
-                    ok = false;
-                    break;
+                if (!ok) {
+                    *abort_flag = 1;
+                    atomicOr(p.status, SK_DEV_TIMEOUT);
+                    if (last >= 0)     // let this thread's MMAs finish before TMEM is freed
+                        mbar_wait_bounded(bar_sfull(last & 1), (last >> 1) & 1, nullptr, kWaitLimit);
                 }
-            }
-            const bool any_mma = last_qk >= 0 || last_pv >= 0;
-            if (any_mma)
-                mma_commit(bar_odone);      // completes once every MMA issued so far has completed
-            if (!ok) {
-                *abort_flag = 1;
-                atomicOr(p.status, SK_DEV_TIMEOUT);
-                // let issued MMAs finish before TMEM is freed
-                if (any_mma)
-                    mbar_wait_bounded(bar_odone, 0, nullptr, kWaitLimit);
+            } else {
+                // PV(i) as soon as the softmax threads have written P(i).
+                for (int i = 0; i < ntiles && ok; ++i) {
+                    ok = mbar_wait_bounded(bar_pfull(i & 1), (i >> 1) & 1, abort_flag, kWaitLimit);
+                    if (!ok)
+                        break;
+                    tc_fence_after();
+                    const uint32_t so = (uint32_t)((i % C::kStages) * kStageBytes);    // P^T over the dead K area
+#pragma unroll
+                    for (int k = 0; k < kPagesPerTile; ++k)
+                        mma_f16_ss(tmem_o, adv(d_v0, so + k * kChunkBytes), adv(d_p0, so + k * kChunkBytes), idesc_pv,
+                                   (i > 0 || k > 0) ? 1u : 0u);
+                    // p_free before empty: a stage freed (and refilled) implies its p_free arrival
+                    mma_commit(bar_pfree(i & 1));
+                    mma_commit(bar_empty(i % C::kStages));
+                    last = i;
+                    *pv_issued = i + 1;
+                }
+                if (last >= 0)
+                    mma_commit(bar_odone);   // completes once every PV issued has completed
+                if (!ok) {
+                    *abort_flag = 1;
+                    atomicOr(p.status, SK_DEV_TIMEOUT);
+                    if (last >= 0)
+                        mbar_wait_bounded(bar_odone, 0, nullptr, kWaitLimit);
+                }
             }
         }
         __syncwarp();
     } else {
-        // ================================================================ softmax warpgroup
-        const int tw = warp - kSoftmaxWarp0;           // 0..3 within the group
-        const int quarter = warp & 3;                  // TMEM lane quarter this warp may access
-        const int tau = quarter * 32 + lane;           // token row (S) / dimension (O) of this thread
+        // ================================================================ softmax warpgroups
+        // Group g owns query rows [g*RH, (g+1)*RH): their S and O columns, running max, row
+        // sums and P entries, so the two groups never wait for each other.
+        constexpr int RH = C::kRH;
+        constexpr int kLd = RH >= 32 ? 32 : RH;                // TMEM columns per load
+        const int wg = (warp - kSoftmaxWarp0) >> 2;            // softmax group
+        const int tw = (warp - kSoftmaxWarp0) & 3;             // warp within the group
+        const int r0 = wg * RH;                                // first row of the group
+        const uint32_t bar_id = 1 + wg;                        // named barrier of the group
+        const int quarter = warp & 3;                          // TMEM lane quarter this warp may access
+        const int tau = quarter * 32 + lane;                   // token row (S) / dimension (O) of this thread
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const int tid = tw * 32 + lane;
         const int causal_base = w.L - w.q_len;
         const int last_page_end = (w.L + kPage - 1) / kPage * kPage;
-        float lsum[RP];
-#pragma unroll
-        for (int r = 0; r < RP; ++r)
-            lsum[r] = 0.f;
         bool failed = false;
+        volatile int *gflags = flags + wg * 12;
+        float *gred = red + wg * (4 * 32);
+        // fp8: dims [64 wg, 64 wg + 64) of this token's V row of tile jt, e4m3 codes (TMA-swizzled)
+        // -> f16 in the MN-major operand layout (atom wg); rows past L become zeros.  The codes were
+        // written by the TMA: they are acquired through the stage's barrier, whose phase for tile jt
+        // cannot advance before tile jt's PV has run.  Returns false if that wait gave up.
+        auto convert_v = [&](int jt) -> bool {
+            const int stv = jt % C::kStages;
+            const bool got = mbar_wait_bounded(bar_full(stv), (jt / C::kStages) & 1, abort_flag, kWaitLimit);
+            const int tokv = k0 + jt * kTokTile + tau;
+            const bool zero = !got || (tokv >= w.L && tokv < last_page_end);
+            const uint8_t *vraw = smem + stv * kStageBytes + kChunkRegion + (tau >> 4) * kChunkBytes + (tau & 15) * 128;
+            uint8_t *atom = smem + stv * kStageBytes + C::kOffV + wg * kChunkRegion + (tau >> 3) * 1024 + (tau & 7) * 128;
+#pragma unroll
+            for (int uu = 0; uu < 4; ++uu) {
+                const int u = 4 * wg + uu;                                                    // dims 16u..16u+15
+                uint4 cv = *reinterpret_cast<const uint4 *>(vraw + ((u ^ (tau & 7)) << 4));
+                if (zero)
+                    cv = make_uint4(0u, 0u, 0u, 0u);
+                const uint32_t wv[4] = {cv.x, cv.y, cv.z, cv.w};
+                uint32_t hv[8];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    hv[2 * k] = e4m3x2_to_f16x2(wv[k]);
+                    hv[2 * k + 1] = e4m3x2_to_f16x2(wv[k] >> 16);
+                }
+                // f16 dims 16u..16u+7 and 16u+8..16u+15: units 2 uu and 2 uu + 1 of the atom row
+                const int u0 = 2 * uu;
+                *reinterpret_cast<uint4 *>(atom + ((u0 ^ (tau & 7)) << 4)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+                *reinterpret_cast<uint4 *>(atom + (((u0 + 1) ^ (tau & 7)) << 4)) = make_uint4(hv[4], hv[5], hv[6], hv[7]);
+            }
+            return got;
+        };
+        if constexpr (FP8) {
+            if (ntiles > 0 && !convert_v(0))
+                failed = true;
+        }
+        float lsum[RH];
+#pragma unroll
+        for (int r = 0; r < RH; ++r)
+            lsum[r] = 0.f;
 
         for (int j = 0; j < ntiles; ++j) {
             const int b = j & 1;
             const int st = j % C::kStages;
-            float x[RP];
+            float x[RH];
             bool ok = !failed && mbar_wait_bounded(bar_sfull(b), (j >> 1) & 1, abort_flag, kWaitLimit);
             ok = __all_sync(kFull, ok);          // tcgen05.ld is warp-collective
             if (ok) {
                 tc_fence_after();
 #pragma unroll
-                for (int c = 0; c < RP; c += (RP >= 32 ? 32 : 16))
-                    tmem_ld32<(RP >= 32 ? 32 : 16)>(tmem_s0 + b * RP + c + lane_off, x + c);
+                for (int c = 0; c < RH; c += kLd)
+                    tmem_ld32<kLd>(tmem_s0 + b * RP + r0 + c + lane_off, x + c);
                 tmem_wait_ld();
             }
             tc_fence_before();
@@ -512,9 +578,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             // (padding rows r >= R have zero Q, so their scores are 0: harmless, and never written out)
             if (ok && tok < k1 && rmin == 0) {
 #pragma unroll
-                for (int r = 0; r < RP; r += 4) {
-                    const float4 t = *reinterpret_cast<const float4 *>(m_thr + r);
-                    const float4 c = *reinterpret_cast<const float4 *>(crow + r);
+                for (int r = 0; r < RH; r += 4) {
+                    const float4 t = *reinterpret_cast<const float4 *>(m_thr + r0 + r);
+                    const float4 c = *reinterpret_cast<const float4 *>(crow + r0 + r);
                     x[r] *= c.x;
                     x[r + 1] *= c.y;
                     x[r + 2] *= c.z;
@@ -524,67 +590,68 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             } else {
                 const bool tok_vis = ok && tok < k1;
 #pragma unroll
-                for (int r = 0; r < RP; ++r) {
-                    x[r] = (tok_vis && r >= rmin && r < R) ? x[r] * crow[r] : -CUDART_INF_F;
-                    need |= x[r] > m_thr[r];
+                for (int r = 0; r < RH; ++r) {
+                    const int rg = r0 + r;
+                    x[r] = (tok_vis && rg >= rmin && rg < R) ? x[r] * crow[rg] : -CUDART_INF_F;
+                    need |= x[r] > m_thr[rg];
                 }
             }
-            // group-wide decision: rescale needed? a wait failed?  (flags double-buffered by tile parity)
+            // group decision: rescale needed? a wait failed?  (flags double-buffered by tile parity)
             const unsigned any_need = __any_sync(kFull, need);
             const unsigned any_fail = __any_sync(kFull, !ok);
             if (lane == 0)
-                flags[4 * b + tw] = (any_need ? 1 : 0) | (any_fail ? 2 : 0);
-            named_bar_sync(1, 128);
-            const int fl = flags[4 * b] | flags[4 * b + 1] | flags[4 * b + 2] | flags[4 * b + 3];
+                gflags[4 * b + tw] = (any_need ? 1 : 0) | (any_fail ? 2 : 0);
+            named_bar_sync(bar_id, 128);
+            const int fl = gflags[4 * b] | gflags[4 * b + 1] | gflags[4 * b + 2] | gflags[4 * b + 3];
             if (fl & 2) {
                 failed = true;
                 break;
             }
             if (fl & 1) {
-                // exact tile max per row across the 128 threads, 32 rows (or all 16) at a time
-                constexpr int kRc = RP >= 32 ? 32 : RP;
+                // exact tile max of the group's rows across its 128 threads
+                constexpr int kRc = RH >= 32 ? 32 : RH;
 #pragma unroll
-                for (int c0 = 0; c0 < RP; c0 += kRc) {
+                for (int c0 = 0; c0 < RH; c0 += kRc) {
                     float v[kRc];
 #pragma unroll
                     for (int r = 0; r < kRc; ++r)
                         v[r] = x[c0 + r];
                     warp_transpose_reduce<kRc, true>(v, lane);
-                    red[tw * 64 + c0 + reduce_row0<kRc>(lane)] = v[0];
+                    gred[tw * 32 + c0 + reduce_row0<kRc>(lane)] = v[0];
                 }
-                named_bar_sync(1, 128);
-                if (tid < RP) {
-                    const float mt = fmaxf(fmaxf(red[tid], red[64 + tid]), fmaxf(red[128 + tid], red[192 + tid]));
-                    const float mo = m_run[tid];
+                named_bar_sync(bar_id, 128);
+                if (tid < RH) {
+                    const int rg = r0 + tid;
+                    const float mt = fmaxf(fmaxf(gred[tid], gred[32 + tid]), fmaxf(gred[64 + tid], gred[96 + tid]));
+                    const float mo = m_run[rg];
                     const float mn = fmaxf(mo, mt);
-                    alpha_s[tid] = (mo == -CUDART_INF_F) ? 0.f : exp2f(mo - mn);
-                    m_run[tid] = mn;
-                    m_thr[tid] = mn + kRescaleLog2;
-                    m_sub[tid] = mn == -CUDART_INF_F ? 0.f : mn;
+                    alpha_s[rg] = (mo == -CUDART_INF_F) ? 0.f : exp2f(mo - mn);
+                    m_run[rg] = mn;
+                    m_thr[rg] = mn + kRescaleLog2;
+                    m_sub[rg] = mn == -CUDART_INF_F ? 0.f : mn;
                 }
-                named_bar_sync(1, 128);
+                named_bar_sync(bar_id, 128);
 #pragma unroll
-                for (int r = 0; r < RP; ++r)
-                    lsum[r] *= alpha_s[r];
+                for (int r = 0; r < RH; ++r)
+                    lsum[r] *= alpha_s[r0 + r];
                 if (j > 0) {
                     // O holds tiles < j: wait for PV(j-1), then rescale this thread's dimension.
-                    // p_free completes once per PV; S(j) being ready means PV(j-2) is done (it was
-                    // issued before QK(j)) and PV(j) cannot start before this tile's P, so the
-                    // parity of PV(j-1) is unambiguous here.
-                    bool okp = mbar_wait_bounded(bar_pfree, (j - 1) & 1, abort_flag, kWaitLimit);
+                    // p_free[b] completes once per PV of a tile of parity b.  Tile j has landed, so
+                    // PV(j - kStages) (which freed its stage) and every earlier PV are done, and PV(j+1)
+                    // cannot start before P(j+1): the phase of PV(j-1) is unambiguous here.
+                    bool okp = mbar_wait_bounded(bar_pfree((j - 1) & 1), ((j - 1) >> 1) & 1, abort_flag, kWaitLimit);
                     okp = __all_sync(kFull, okp);    // tcgen05.ld/st are warp-collective
                     if (okp) {
                         tc_fence_after();
-                        constexpr int kOc = RP >= 32 ? 32 : 16;
 #pragma unroll
-                        for (int c = 0; c < RP; c += kOc) {
-                            float o[kOc];
-                            tmem_ld32<kOc>(tmem_o + c + lane_off, o);
+                        for (int c = 0; c < RH; c += kLd) {
+                            float o[kLd];
+                            tmem_ld32<kLd>(tmem_o + r0 + c + lane_off, o);
                             tmem_wait_ld();
 #pragma unroll
-                            for (int r = 0; r < kOc; ++r)
-                                o[r] *= alpha_s[c + r];
-                            tmem_st32<kOc>(tmem_o + c + lane_off, o);
+                            for (int r = 0; r < kLd; ++r)
+                                o[r] *= alpha_s[r0 + c + r];
+                            tmem_st32<kLd>(tmem_o + r0 + c + lane_off, o);
                         }
                         tmem_wait_st();
                     } else {
@@ -598,9 +665,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                 // MN-major, 128-byte swizzle, 16-byte unit u of row tau stored at u ^ (tau % 8)
                 uint8_t *prow = smem + st * kStageBytes + (tau >> 3) * 1024 + (tau & 7) * 128;
 #pragma unroll
-                for (int u = 0; u < RP / 8; ++u) {
-                    const float4 ma = *reinterpret_cast<const float4 *>(m_sub + 8 * u);
-                    const float4 mb = *reinterpret_cast<const float4 *>(m_sub + 8 * u + 4);
+                for (int u = 0; u < RH / 8; ++u) {
+                    const float4 ma = *reinterpret_cast<const float4 *>(m_sub + r0 + 8 * u);
+                    const float4 mb = *reinterpret_cast<const float4 *>(m_sub + r0 + 8 * u + 4);
                     const float mm[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
                     uint32_t pk[4];
 #pragma unroll
@@ -612,43 +679,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                         lsum[r + 1] += p1;
                         pk[e] = FP8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
                     }
-                    *reinterpret_cast<uint4 *>(prow + ((u ^ (tau & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    const int ug = r0 / 8 + u;                 // unit of the row
+                    *reinterpret_cast<uint4 *>(prow + ((ug ^ (tau & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 }
                 const bool tail_row = tok >= w.L && tok < last_page_end;   // past L in the last page: anything
-                if constexpr (FP8) {
-                    // this token's V row: e4m3 codes (TMA-swizzled) -> f16 in the MN-major operand layout;
-                    // rows past L are written as zeros.  The codes were written by the TMA: acquire them
-                    // through the stage's barrier (its phase for this tile is complete and cannot advance
-                    // before this tile's PV has run).
-                    if (!mbar_wait_bounded(bar_full(st), (j / C::kStages) & 1, abort_flag, kWaitLimit))
-                        failed = true;
-                    const uint8_t *vraw = smem + st * kStageBytes + kChunkRegion + (tau >> 4) * kChunkBytes + (tau & 15) * 128;
-                    uint8_t *vrow = smem + st * kStageBytes + C::kOffV + (tau >> 3) * 1024 + (tau & 7) * 128;
+                if (!FP8 && tail_row) {
+                    // V dims [64 wg, 64 wg + 64) of this row: chunk 2 + wg
+                    uint8_t *vrow = smem + st * kStageBytes + C::kOffV + wg * kChunkRegion + (tau >> 4) * kChunkBytes +
+                                    (tau & 15) * 128;
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        uint4 cv = *reinterpret_cast<const uint4 *>(vraw + ((u ^ (tau & 7)) << 4));   // dims 16u..16u+15
-                        if (tail_row || failed)
-                            cv = make_uint4(0u, 0u, 0u, 0u);
-                        const uint32_t wv[4] = {cv.x, cv.y, cv.z, cv.w};
-                        uint32_t hv[8];
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            hv[2 * k] = e4m3x2_to_f16x2(wv[k]);
-                            hv[2 * k + 1] = e4m3x2_to_f16x2(wv[k] >> 16);
-                        }
-                        // f16 dims 16u..16u+7 and 16u+8..16u+15: atom (16u)/64, units 2(u%4) and 2(u%4)+1
-                        uint8_t *atom = vrow + (u >> 2) * kChunkRegion;
-                        const int u0 = 2 * (u & 3);
-                        *reinterpret_cast<uint4 *>(atom + ((u0 ^ (tau & 7)) << 4)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-                        *reinterpret_cast<uint4 *>(atom + (((u0 + 1) ^ (tau & 7)) << 4)) = make_uint4(hv[4], hv[5], hv[6], hv[7]);
-                    }
-                } else if (tail_row) {
-                    uint8_t *vrow = smem + st * kStageBytes + C::kOffV + (tau >> 4) * kChunkBytes + (tau & 15) * 128;
-#pragma unroll
-                    for (int c = 0; c < 2; ++c)
-#pragma unroll
-                        for (int u = 0; u < 8; ++u)
-                            *reinterpret_cast<uint4 *>(vrow + c * kChunkRegion + u * 16) = make_uint4(0u, 0u, 0u, 0u);
+                    for (int u = 0; u < 8; ++u)
+                        *reinterpret_cast<uint4 *>(vrow + u * 16) = make_uint4(0u, 0u, 0u, 0u);
                 }
                 fence_proxy_async_smem();
             }
@@ -656,13 +697,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(bar_pfull(b));
+            // fp8: the next tile's V conversion fills the wait for its S (its stage is free once it
+            // has landed); the fence before that tile's P_full publishes it to the tensor core
+            if (FP8 && !failed && j + 1 < ntiles && !convert_v(j + 1))
+                failed = true;
             if (failed) {
                 // the next tile's group decision propagates the failure
                 *abort_flag = 1;
             }
         }
 
-        // ---- epilogue: O complete?  then row sums across the 128 threads and the partials
+        // ---- epilogue: O complete?  then row sums across the group's threads and the partials
         // (p_free cannot tell PV(last) from PV(last-1) here: both may still be running)
         bool okf = !failed;
         if (okf && ntiles > 0)
@@ -671,45 +716,44 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
         {
             const unsigned any_fail = __any_sync(kFull, !okf);
             if (lane == 0)
-                flags[8 + tw] = any_fail ? 2 : 0;
+                gflags[8 + tw] = any_fail ? 2 : 0;
         }
-        named_bar_sync(1, 128);
-        const bool write = ((flags[8] | flags[9] | flags[10] | flags[11]) & 2) == 0;
+        named_bar_sync(bar_id, 128);
+        const bool write = ((gflags[8] | gflags[9] | gflags[10] | gflags[11]) & 2) == 0;
         {
-            constexpr int kRc = RP >= 32 ? 32 : RP;
+            constexpr int kRc = RH >= 32 ? 32 : RH;
 #pragma unroll
-            for (int c0 = 0; c0 < RP; c0 += kRc) {
+            for (int c0 = 0; c0 < RH; c0 += kRc) {
                 float v[kRc];
 #pragma unroll
                 for (int r = 0; r < kRc; ++r)
                     v[r] = lsum[c0 + r];
                 warp_transpose_reduce<kRc, false>(v, lane);
-                red[tw * 64 + c0 + reduce_row0<kRc>(lane)] = v[0];
+                gred[tw * 32 + c0 + reduce_row0<kRc>(lane)] = v[0];
             }
         }
-        named_bar_sync(1, 128);
-        if (tid < RP)
-            alpha_s[tid] = (red[tid] + red[64 + tid]) + (red[128 + tid] + red[192 + tid]);
-        named_bar_sync(1, 128);
+        named_bar_sync(bar_id, 128);
+        if (tid < RH)
+            alpha_s[r0 + tid] = (gred[tid] + gred[32 + tid]) + (gred[64 + tid] + gred[96 + tid]);
+        named_bar_sync(bar_id, 128);
         if (write) {
             if (ntiles > 0)
                 tc_fence_after();
             const long long seg_base = (long long)w.g * p.H_q + h * p.G;
-            constexpr int kOc = RP >= 32 ? 32 : 16;
 #pragma unroll
-            for (int c = 0; c < RP; c += kOc) {
-                float o[kOc];
+            for (int c = 0; c < RH; c += kLd) {
+                float o[kLd];
                 if (ntiles > 0) {
-                    tmem_ld32<kOc>(tmem_o + c + lane_off, o);
+                    tmem_ld32<kLd>(tmem_o + r0 + c + lane_off, o);
                     tmem_wait_ld();
                 } else {
 #pragma unroll
-                    for (int r = 0; r < kOc; ++r)
+                    for (int r = 0; r < kLd; ++r)
                         o[r] = 0.f;
                 }
 #pragma unroll
-                for (int rr = 0; rr < kOc; ++rr) {
-                    const int r = c + rr;
+                for (int rr = 0; rr < kLd; ++rr) {
+                    const int r = r0 + c + rr;
                     if (r < R) {
                         const int jq = r / p.G, i = r - jq * p.G;
                         const long long slot = (long long)(w.tok0 + jq) * p.seg_max * p.H_q + seg_base + i;

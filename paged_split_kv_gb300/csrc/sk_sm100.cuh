@@ -135,6 +135,18 @@ template <int N>
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v);
 
 template <>
+__device__ __forceinline__ void tmem_ld32<8>(uint32_t taddr, float *v)
+{
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        v[i] = __uint_as_float(r[i]);
+}
+
+template <>
 __device__ __forceinline__ void tmem_ld32<16>(uint32_t taddr, float *v)
 {
     uint32_t r[16];
@@ -167,6 +179,16 @@ __device__ __forceinline__ void tmem_ld32<32>(uint32_t taddr, float *v)
 
 template <int N>
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float *v);
+
+template <>
+__device__ __forceinline__ void tmem_st32<8>(uint32_t taddr, const float *v)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+                 "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+                 "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+                 "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
+                 : "memory");
+}
 
 template <>
 __device__ __forceinline__ void tmem_st32<16>(uint32_t taddr, const float *v)
