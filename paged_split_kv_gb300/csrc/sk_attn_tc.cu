@@ -58,8 +58,7 @@ using namespace sm100;
 
 constexpr int kTokTile = 128;                       // tokens per tile (MMA M)
 constexpr int kPagesPerTile = kTokTile / kPage;     // 8
-constexpr int kChunkBytes = kPage * 128;            // one page x 128-byte rows: 2 KB
-constexpr int kChunkRegion = kPagesPerTile * kChunkBytes;   // 16 KB: 128 token rows of 128 B
+constexpr int kChunkRegion = kTokTile * 128;        // 16 KB: 128 token rows of 128 B
 constexpr int kStageBytes = 4 * kChunkRegion;       // 64 KB
 constexpr int kSoftmaxWarp0 = 2;
 constexpr int kSoftmaxGroups = 2;                   // warpgroups splitting the query rows
@@ -71,9 +70,14 @@ constexpr long long kWaitLimit = 4000000000LL;      // cycles (~2 s)
 constexpr uint32_t kFull = 0xffffffffu;
 constexpr int kMaxSmem = 232448;                    // 227 KB per CTA
 
-// Stage layout (64 KB):
-//   bf16: [0,16K) K dims 0-63 (later P^T) | [16K,32K) K dims 64-127 | [32K,48K) V dims 0-63 | [48K,64K) V dims 64-127
-//   fp8:  [0,16K) K e4m3 (later P^T)      | [16K,32K) V e4m3         | [32K,48K) V f16 dims 0-63 | [48K,64K) V f16 64-127
+// Stage layout.  One TMA copy per page brings its 16 token rows as two 8-token
+// groups, each group as its 128-byte chunks of the row, each chunk an 8 x 128 B
+// swizzle atom: token t's chunk c sits at (t / 8) * kGroupBytes + c * 1 KB +
+// (t % 8) * 128.  Every chunk is then a K-major (or MN-major) 128-byte-swizzled
+// operand over the 128 tokens whose 8-row groups are kGroupBytes apart.
+//   bf16: groups of 4 KB: chunks K 0-63 (later P^T), K 64-127, V 0-63, V 64-127
+//   fp8:  groups of 2 KB in [0,32K): chunks K codes (later P^T), V codes;
+//         [32K,48K) V f16 dims 0-63 | [48K,64K) V f16 dims 64-127 (8-token atoms 1 KB apart)
 template <int RP, bool FP8>
 struct Cfg {
     static_assert(RP == 16 || RP == 32 || RP == 64, "rows per work item: 16, 32 or 64");
@@ -87,7 +91,13 @@ struct Cfg {
     static constexpr int kSmemBytes = kOffMisc + kMiscBytes;
     static constexpr int kTmemCols = (3 * RP <= 64) ? 64 : (3 * RP <= 128) ? 128 : 256;
     static constexpr uint32_t kTxBytes = FP8 ? 2 * kChunkRegion : 4 * kChunkRegion;   // bytes the TMA brings per stage
-    static constexpr int kOffV = 2 * kChunkRegion;           // V operand (bf16 chunks 2-3, or converted f16)
+    static constexpr int kGroupBytes = FP8 ? 2048 : 4096;     // one 8-token group of the raw rows
+    static constexpr int kPageBytes = 2 * kGroupBytes;        // one page (one TMA copy)
+    // V operand: bf16 chunks 2-3 of the raw rows (atoms 1 KB apart along the dimensions,
+    // groups kGroupBytes apart), or the converted f16 (atoms 16 KB apart, groups 1 KB apart)
+    static constexpr int kOffV = FP8 ? 2 * kChunkRegion : 2048;
+    static constexpr int kVDimStride = FP8 ? kChunkRegion : 1024;
+    static constexpr int kVGroupStride = FP8 ? 1024 : kGroupBytes;
     // misc area
     static constexpr int kBarFull = 0;                       // [kStages]
     static constexpr int kBarEmpty = 8 * kStages;            // [kStages]
@@ -375,22 +385,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                 mbar_arrive_expect_tx(bar_full(st), C::kTxBytes);
             __syncwarp();
             if (lane < kPagesPerTile) {
-                int y = -kPage;                       // whole box out of bounds: zero fill
+                int grp = -2;                         // whole box out of bounds: zero fill
                 if (pg < page_end) {
                     if (blk >= 0 && blk < p.num_blocks)
-                        y = (blk * p.H_kv + h) * kPage;
+                        grp = (blk * p.H_kv + h) * 2;
                     else
                         atomicOr(p.status, SK_DEV_BAD_BLOCK);
                 }
-                const uint32_t dst = stage(st) + lane * kChunkBytes;
-                if constexpr (FP8) {
-                    tma_load_2d(dst, &kv_map, 0, y, bar_full(st));                    // K codes
-                    tma_load_2d(dst + kChunkRegion, &kv_map, 128, y, bar_full(st));   // V codes
-                } else {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        tma_load_2d(dst + c * kChunkRegion, &kv_map, c * 64, y, bar_full(st));
-                }
+                tma_load_4d(stage(st) + lane * C::kPageBytes, &kv_map, 0, 0, 0, grp, bar_full(st));
             }
             issued = j + 1;
         }
@@ -411,9 +413,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
         if (lane == 0) {
             constexpr uint32_t idesc_qk = FP8 ? idesc_e4m3_f32(kTokTile, RP, 0, 0) : idesc_bf16_f32(kTokTile, RP, 0, 0);
             constexpr uint32_t idesc_pv = FP8 ? idesc_f16_f32(kTokTile, RP, 1, 1) : idesc_bf16_f32(kTokTile, RP, 1, 1);
-            const uint64_t d_kv0 = smem_desc_sw128(stage(0), 16, 1024);                    // K-major K tile
-            const uint64_t d_v0 = smem_desc_sw128(stage(0) + C::kOffV, kChunkRegion, 1024);  // MN-major V^T
-            const uint64_t d_p0 = smem_desc_sw128(stage(0), 1024, 1024);                   // MN-major P^T
+            const uint64_t d_kv0 = smem_desc_sw128(stage(0), 16, C::kGroupBytes);           // K-major K tile
+            const uint64_t d_v0 = smem_desc_sw128(stage(0) + C::kOffV, C::kVDimStride, C::kVGroupStride);  // MN-major V^T
+            const uint64_t d_p0 = smem_desc_sw128(stage(0), 1024, C::kGroupBytes);          // MN-major P^T
             const uint64_t d_q0 = smem_desc_sw128(q_s, 16, 1024);                          // K-major Q
             auto adv = [](uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); };
             bool ok = true;
@@ -450,7 +452,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                     } else {
 #pragma unroll
                         for (int k = 0; k < kHeadDim / 16; ++k) {
-                            const uint32_t off = (uint32_t)((k >> 2) * kChunkRegion + (k & 3) * 32);
+                            const uint32_t off = (uint32_t)((k >> 2) * 1024 + (k & 3) * 32);
                             const uint32_t qoff = (uint32_t)((k >> 2) * (RP * 128) + (k & 3) * 32);
                             mma_f16_ss(tmem_s0 + b * RP, adv(d_kv0, so + off), adv(d_q0, qoff), idesc_qk, k > 0 ? 1u : 0u);
                         }
@@ -474,7 +476,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                     const uint32_t so = (uint32_t)((i % C::kStages) * kStageBytes);    // P^T over the dead K area
 #pragma unroll
                     for (int k = 0; k < kPagesPerTile; ++k)
-                        mma_f16_ss(tmem_o, adv(d_v0, so + k * kChunkBytes), adv(d_p0, so + k * kChunkBytes), idesc_pv,
+                        mma_f16_ss(tmem_o, adv(d_v0, so + k * 2 * C::kVGroupStride), adv(d_p0, so + k * 2 * C::kGroupBytes), idesc_pv,
                                    (i > 0 || k > 0) ? 1u : 0u);
                     // p_free before empty: a stage freed (and refilled) implies its p_free arrival
                     mma_commit(bar_pfree(i & 1));
@@ -521,7 +523,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             const bool got = mbar_wait_bounded(bar_full(stv), (jt / C::kStages) & 1, abort_flag, kWaitLimit);
             const int tokv = k0 + jt * kTokTile + tau;
             const bool zero = !got || (tokv >= w.L && tokv < last_page_end);
-            const uint8_t *vraw = smem + stv * kStageBytes + kChunkRegion + (tau >> 4) * kChunkBytes + (tau & 15) * 128;
+            const uint8_t *vraw = smem + stv * kStageBytes + (tau >> 3) * C::kGroupBytes + 1024 + (tau & 7) * 128;
             uint8_t *atom = smem + stv * kStageBytes + C::kOffV + wg * kChunkRegion + (tau >> 3) * 1024 + (tau & 7) * 128;
 #pragma unroll
             for (int uu = 0; uu < 4; ++uu) {
@@ -663,7 +665,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                 // probabilities against the running max (masked entries are -inf -> 0), written as
                 // this token's row of P^T over the tile's K area, which QK(j) no longer needs:
                 // MN-major, 128-byte swizzle, 16-byte unit u of row tau stored at u ^ (tau % 8)
-                uint8_t *prow = smem + st * kStageBytes + (tau >> 3) * 1024 + (tau & 7) * 128;
+                uint8_t *prow = smem + st * kStageBytes + (tau >> 3) * C::kGroupBytes + (tau & 7) * 128;
 #pragma unroll
                 for (int u = 0; u < RH / 8; ++u) {
                     const float4 ma = *reinterpret_cast<const float4 *>(m_sub + r0 + 8 * u);
@@ -685,8 +687,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                 const bool tail_row = tok >= w.L && tok < last_page_end;   // past L in the last page: anything
                 if (!FP8 && tail_row) {
                     // V dims [64 wg, 64 wg + 64) of this row: chunk 2 + wg
-                    uint8_t *vrow = smem + st * kStageBytes + C::kOffV + wg * kChunkRegion + (tau >> 4) * kChunkBytes +
-                                    (tau & 15) * 128;
+                    uint8_t *vrow = smem + st * kStageBytes + C::kOffV + wg * 1024 + (tau >> 3) * C::kGroupBytes +
+                                    (tau & 7) * 128;
 #pragma unroll
                     for (int u = 0; u < 8; ++u)
                         *reinterpret_cast<uint4 *>(vrow + u * 16) = make_uint4(0u, 0u, 0u, 0u);
@@ -819,7 +821,7 @@ int attn_tc_rows(int kv_dtype, int rows_max, long long num_blocks, int H_kv)
 {
     if ((kv_dtype != SK_KV_BF16 && kv_dtype != SK_KV_FP8_E4M3) || rows_max < 1 || rows_max > 64)
         return 0;
-    if (num_blocks * H_kv * kPage > 0x7FFFFFFFLL)
+    if (num_blocks * H_kv * 2 > 0x7FFFFFFFLL)
         return 0;
     return rows_max <= 16 ? 16 : rows_max <= 32 ? 32 : 64;
 }
@@ -831,12 +833,16 @@ cudaError_t launch_attn_tc(const AttnParams &p, int kv_dtype, int rp, cudaStream
         return cudaErrorNotSupported;
     const bool fp8 = kv_dtype == SK_KV_FP8_E4M3;
     CUtensorMap map;
-    // one row of 2 * 128 elements (K | V of one token of one head) per (block, head, token)
-    const cuuint64_t dims[2] = {(cuuint64_t)(2 * kHeadDim), (cuuint64_t)p.num_blocks * p.H_kv * kPage};
-    const cuuint64_t strides[1] = {(cuuint64_t)(2 * kHeadDim * (fp8 ? 1 : 2))};
-    const cuuint32_t box[2] = {fp8 ? 128u : 64u, (cuuint32_t)kPage};     // 128-byte box rows
-    const cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(&map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+    // The pages [blocks][heads][16 tokens][K | V] seen as 4-D: (128 bytes of a row, token within an
+    // 8-token group, 128-byte chunk of the row, 8-token group across all pages).  One box is a whole
+    // page of one head and lands group by group, chunk by chunk, as 8 x 128 B swizzle atoms.
+    const cuuint64_t row_bytes = (cuuint64_t)(2 * kHeadDim * (fp8 ? 1 : 2));
+    const cuuint32_t nchunks = (cuuint32_t)(row_bytes / 128);
+    const cuuint64_t dims[4] = {(cuuint64_t)(fp8 ? 128 : 64), 8, nchunks, (cuuint64_t)p.num_blocks * p.H_kv * 2};
+    const cuuint64_t strides[3] = {row_bytes, 128, 8 * row_bytes};
+    const cuuint32_t box[4] = {fp8 ? 128u : 64u, 8, nchunks, 2};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(&map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
                      const_cast<void *>(p.kv), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
