@@ -85,7 +85,6 @@ struct Cfg {
     static constexpr int kMiscBytes = 4096;
     static constexpr int kRH = RP / kSoftmaxGroups;          // rows per softmax warpgroup
     static constexpr int kStages = (3 * kStageBytes + kQBytes + kMiscBytes <= kMaxSmem) ? 3 : 2;
-    static_assert(kStages <= 3, "p_free phases rely on PV(j - 3) being done once tile j has landed");
     static constexpr int kOffQ = kStages * kStageBytes;
     static constexpr int kOffMisc = kOffQ + kQBytes;
     static constexpr int kSmemBytes = kOffMisc + kMiscBytes;
@@ -104,8 +103,7 @@ struct Cfg {
     static constexpr int kBarSFull = 16 * kStages;           // [2]
     static constexpr int kBarSFree = kBarSFull + 16;         // [2]
     static constexpr int kBarPFull = kBarSFree + 16;         // [2], by tile parity
-    static constexpr int kBarPFree = kBarPFull + 16;         // [2], by tile parity
-    static constexpr int kBarODone = kBarPFree + 16;         // committed once, after the last PV
+    static constexpr int kBarODone = kBarPFull + 16;         // committed once, after the last PV
     static constexpr int kTmemSlot = kBarODone + 8;
     static constexpr int kAbort = kTmemSlot + 4;
     static constexpr int kPvIssued = kAbort + 4;             // int: PVs issued so far (written by the PV thread)
@@ -255,7 +253,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
     auto bar_sfull = [&](int b) { return mbase + C::kBarSFull + 8 * b; };
     auto bar_sfree = [&](int b) { return mbase + C::kBarSFree + 8 * b; };
     auto bar_pfull = [&](int b) { return mbase + C::kBarPFull + 8 * b; };
-    auto bar_pfree = [&](int b) { return mbase + C::kBarPFree + 8 * b; };
     volatile int *pv_issued = reinterpret_cast<volatile int *>(misc + C::kPvIssued);
     const uint32_t bar_odone = mbase + C::kBarODone;
     const uint32_t q_s = sbase + C::kOffQ;
@@ -275,8 +272,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             mbar_init(bar_sfree(b), kSoftmaxWarps);
             mbar_init(bar_pfull(b), kSoftmaxWarps);
         }
-        mbar_init(bar_pfree(0), 1);
-        mbar_init(bar_pfree(1), 1);
         mbar_init(bar_odone, 1);
         *abort_flag = 0;
         *pv_issued = 0;
@@ -406,92 +401,98 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
         }
     } else if (warp == 1 || warp == kPvWarp) {
         // ================================================================ MMA issuers
+        // Whole warps run these loops; one elected lane issues each MMA and commit.
         // QK: bf16 kind::f16, 8 steps of 16 dims; fp8 kind::f8f6f4, 4 steps of 32 dims per Q term.
-        // PV: V^T (MN-major, two 64-dim atoms 16 KB apart) x P^T (MN-major), 8 steps of 16 tokens.
+        // PV: V^T (MN-major, two 64-dim atoms) x P^T (MN-major), 8 steps of 16 tokens.
         // Descriptors are built once for stage 0 / Q; an operand elsewhere is the same descriptor
         // advanced by (byte offset >> 4) in its start-address field (shared addresses < 256 KB).
-        if (lane == 0) {
-            constexpr uint32_t idesc_qk = FP8 ? idesc_e4m3_f32(kTokTile, RP, 0, 0) : idesc_bf16_f32(kTokTile, RP, 0, 0);
-            constexpr uint32_t idesc_pv = FP8 ? idesc_f16_f32(kTokTile, RP, 1, 1) : idesc_bf16_f32(kTokTile, RP, 1, 1);
-            const uint64_t d_kv0 = smem_desc_sw128(stage(0), 16, C::kGroupBytes);           // K-major K tile
-            const uint64_t d_v0 = smem_desc_sw128(stage(0) + C::kOffV, C::kVDimStride, C::kVGroupStride);  // MN-major V^T
-            const uint64_t d_p0 = smem_desc_sw128(stage(0), 1024, C::kGroupBytes);          // MN-major P^T
-            const uint64_t d_q0 = smem_desc_sw128(q_s, 16, 1024);                          // K-major Q
-            auto adv = [](uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); };
-            bool ok = true;
-            int last = -1;
-            if (warp == 1) {
-                // QK(j) once tile j has landed, its S buffer is free, and PV(j-2) is issued.  The last
-                // condition keeps barrier phases unambiguous: P_full[b] cannot run two tiles ahead of
-                // its PV, and the softmax never runs more than one tile ahead of the PVs it waits on.
-                for (int j = 0; j < ntiles && ok; ++j) {
-                    const int st = j % C::kStages, b = j & 1;
-                    ok = mbar_wait_bounded(bar_full(st), (j / C::kStages) & 1, abort_flag, kWaitLimit);
-                    if (ok && j >= 2)
-                        ok = mbar_wait_bounded(bar_sfree(b), ((j - 2) >> 1) & 1, abort_flag, kWaitLimit);
-                    if (ok && *pv_issued < j - 1) {
-                        const long long t0 = clock64();
-                        while (*pv_issued < j - 1) {
-                            if (*abort_flag || clock64() - t0 > kWaitLimit) {
-                                ok = false;
-                                break;
-                            }
+        constexpr uint32_t idesc_qk = FP8 ? idesc_e4m3_f32(kTokTile, RP, 0, 0) : idesc_bf16_f32(kTokTile, RP, 0, 0);
+        constexpr uint32_t idesc_pv = FP8 ? idesc_f16_f32(kTokTile, RP, 1, 1) : idesc_bf16_f32(kTokTile, RP, 1, 1);
+        const uint64_t d_kv0 = smem_desc_sw128(stage(0), 16, C::kGroupBytes);           // K-major K tile
+        const uint64_t d_v0 = smem_desc_sw128(stage(0) + C::kOffV, C::kVDimStride, C::kVGroupStride);  // MN-major V^T
+        const uint64_t d_p0 = smem_desc_sw128(stage(0), 1024, C::kGroupBytes);          // MN-major P^T
+        const uint64_t d_q0 = smem_desc_sw128(q_s, 16, 1024);                          // K-major Q
+        auto adv = [](uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); };
+        bool ok = true;
+        int last = -1;
+        if (warp == 1) {
+            // QK(j) once tile j has landed, its S buffer is free, and PV(j-2) is issued.  The last
+            // condition keeps barrier phases unambiguous: P_full[b] cannot run two tiles ahead of
+            // its PV, and the softmax never runs more than one tile ahead of the PVs it waits on.
+            for (int j = 0; j < ntiles && ok; ++j) {
+                const int st = j % C::kStages, b = j & 1;
+                ok = mbar_wait_bounded(bar_full(st), (j / C::kStages) & 1, abort_flag, kWaitLimit);
+                if (ok && j >= 2)
+                    ok = mbar_wait_bounded(bar_sfree(b), ((j - 2) >> 1) & 1, abort_flag, kWaitLimit);
+                if (ok && *pv_issued < j - 1) {
+                    const long long t0 = clock64();
+                    while (*pv_issued < j - 1) {
+                        if (*abort_flag || clock64() - t0 > kWaitLimit) {
+                            ok = false;
+                            break;
                         }
                     }
-                    if (!ok)
-                        break;
-                    tc_fence_after();
-                    const uint32_t so = (uint32_t)(st * kStageBytes);
-                    if constexpr (FP8) {
-#pragma unroll
-                        for (int t = 0; t < 2; ++t)
-#pragma unroll
-                            for (int k = 0; k < 4; ++k)
-                                mma_f8_ss(tmem_s0 + b * RP, adv(d_kv0, so + k * 32), adv(d_q0, t * (RP * 128) + k * 32),
-                                          idesc_qk, (t > 0 || k > 0) ? 1u : 0u);
-                    } else {
-#pragma unroll
-                        for (int k = 0; k < kHeadDim / 16; ++k) {
-                            const uint32_t off = (uint32_t)((k >> 2) * 1024 + (k & 3) * 32);
-                            const uint32_t qoff = (uint32_t)((k >> 2) * (RP * 128) + (k & 3) * 32);
-                            mma_f16_ss(tmem_s0 + b * RP, adv(d_kv0, so + off), adv(d_q0, qoff), idesc_qk, k > 0 ? 1u : 0u);
-                        }
-                    }
-                    mma_commit(bar_sfull(b));
-                    last = j;
                 }
-                if (!ok) {
+                ok = __all_sync(kFull, ok);
+                if (!ok)
+                    break;
+                tc_fence_after();
+                const uint32_t so = (uint32_t)(st * kStageBytes);
+                if constexpr (FP8) {
+#pragma unroll
+                    for (int t = 0; t < 2; ++t)
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            mma_f8_ss_warp(tmem_s0 + b * RP, adv(d_kv0, so + k * 32), adv(d_q0, t * (RP * 128) + k * 32),
+                                           idesc_qk, (t > 0 || k > 0) ? 1u : 0u);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < kHeadDim / 16; ++k) {
+                        const uint32_t off = (uint32_t)((k >> 2) * 1024 + (k & 3) * 32);
+                        const uint32_t qoff = (uint32_t)((k >> 2) * (RP * 128) + (k & 3) * 32);
+                        mma_f16_ss_warp(tmem_s0 + b * RP, adv(d_kv0, so + off), adv(d_q0, qoff), idesc_qk, k > 0 ? 1u : 0u);
+                    }
+                }
+                mma_commit_warp(bar_sfull(b));
+                last = j;
+            }
+            if (!ok) {
+                if (lane == 0) {
                     *abort_flag = 1;
                     atomicOr(p.status, SK_DEV_TIMEOUT);
-                    if (last >= 0)     // let this thread's MMAs finish before TMEM is freed
-                        mbar_wait_bounded(bar_sfull(last & 1), (last >> 1) & 1, nullptr, kWaitLimit);
                 }
-            } else {
-                // PV(i) as soon as the softmax threads have written P(i).
-                for (int i = 0; i < ntiles && ok; ++i) {
-                    ok = mbar_wait_bounded(bar_pfull(i & 1), (i >> 1) & 1, abort_flag, kWaitLimit);
-                    if (!ok)
-                        break;
-                    tc_fence_after();
-                    const uint32_t so = (uint32_t)((i % C::kStages) * kStageBytes);    // P^T over the dead K area
+                if (last >= 0)     // let this warp's MMAs finish before TMEM is freed
+                    mbar_wait_bounded(bar_sfull(last & 1), (last >> 1) & 1, nullptr, kWaitLimit);
+            }
+        } else {
+            // PV(i) as soon as the softmax threads have written P(i).  Its completion frees the
+            // stage (empty), which is also how the softmax learns that O holds tile i.
+            for (int i = 0; i < ntiles && ok; ++i) {
+                ok = mbar_wait_bounded(bar_pfull(i & 1), (i >> 1) & 1, abort_flag, kWaitLimit);
+                ok = __all_sync(kFull, ok);
+                if (!ok)
+                    break;
+                tc_fence_after();
+                const uint32_t so = (uint32_t)((i % C::kStages) * kStageBytes);    // P^T over the dead K area
 #pragma unroll
-                    for (int k = 0; k < kPagesPerTile; ++k)
-                        mma_f16_ss(tmem_o, adv(d_v0, so + k * 2 * C::kVGroupStride), adv(d_p0, so + k * 2 * C::kGroupBytes), idesc_pv,
-                                   (i > 0 || k > 0) ? 1u : 0u);
-                    // p_free before empty: a stage freed (and refilled) implies its p_free arrival
-                    mma_commit(bar_pfree(i & 1));
-                    mma_commit(bar_empty(i % C::kStages));
-                    last = i;
+                for (int k = 0; k < kPagesPerTile; ++k)
+                    mma_f16_ss_warp(tmem_o, adv(d_v0, so + k * 2 * C::kVGroupStride), adv(d_p0, so + k * 2 * C::kGroupBytes),
+                                    idesc_pv, (i > 0 || k > 0) ? 1u : 0u);
+                mma_commit_warp(bar_empty(i % C::kStages));
+                last = i;
+                __syncwarp();
+                if (lane == 0)
                     *pv_issued = i + 1;
+            }
+            if (last >= 0)
+                mma_commit_warp(bar_odone);   // completes once every PV issued has completed
+            if (!ok) {
+                if (lane == 0) {
+                    *abort_flag = 1;
+                    atomicOr(p.status, SK_DEV_TIMEOUT);
                 }
                 if (last >= 0)
-                    mma_commit(bar_odone);   // completes once every PV issued has completed
-                if (!ok) {
-                    *abort_flag = 1;
-                    atomicOr(p.status, SK_DEV_TIMEOUT);
-                    if (last >= 0)
-                        mbar_wait_bounded(bar_odone, 0, nullptr, kWaitLimit);
-                }
+                    mbar_wait_bounded(bar_odone, 0, nullptr, kWaitLimit);
             }
         }
         __syncwarp();
@@ -638,10 +639,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                     lsum[r] *= alpha_s[r0 + r];
                 if (j > 0) {
                     // O holds tiles < j: wait for PV(j-1), then rescale this thread's dimension.
-                    // p_free[b] completes once per PV of a tile of parity b.  Tile j has landed, so
-                    // PV(j - kStages) (which freed its stage) and every earlier PV are done, and PV(j+1)
-                    // cannot start before P(j+1): the phase of PV(j-1) is unambiguous here.
-                    bool okp = mbar_wait_bounded(bar_pfree((j - 1) & 1), ((j - 1) >> 1) & 1, abort_flag, kWaitLimit);
+                    // PV(i) completes phase i / kStages of empty[i % kStages].  The phase before,
+                    // PV(j-1-kStages), was seen by the producer before it loaded tile j-1, and the one
+                    // after, PV(j-1+kStages), cannot start before P(j+1): PV(j-1)'s is unambiguous here.
+                    const int jp = j - 1;
+                    bool okp = mbar_wait_bounded(bar_empty(jp % C::kStages), (jp / C::kStages) & 1, abort_flag, kWaitLimit);
                     okp = __all_sync(kFull, okp);    // tcgen05.ld/st are warp-collective
                     if (okp) {
                         tc_fence_after();
@@ -710,7 +712,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
         }
 
         // ---- epilogue: O complete?  then row sums across the group's threads and the partials
-        // (p_free cannot tell PV(last) from PV(last-1) here: both may still be running)
+        // (a stage barrier cannot tell PV(last) from PV(last-1) here: both may still be running)
         bool okf = !failed;
         if (okf && ntiles > 0)
             okf = mbar_wait_bounded(bar_odone, 0, abort_flag, kWaitLimit);
