@@ -10,7 +10,7 @@
 // (16, 32 or 64 columns).  S^T and O^T live in tensor memory (TMEM lane =
 // token for S, = dimension for O).
 //
-// Roles (352 threads):
+// Roles (352 threads; 480 with the fp8 converter warps):
 //   warp 0   TMA producer (8 pages per 128-token tile, 128-byte swizzle).
 //            bf16: 4 boxes of 64 elements x 16 rows per page land as
 //            [chunk][page][row][128 B], at once the K-major layout of K
@@ -19,9 +19,9 @@
 //            [page][row][128 B] (K-major, one row is all 128 dims) and V raw.
 //            Pages past the segment end are zero-filled (out-of-bounds box),
 //            so they cost no HBM traffic.
-//   warp 1   allocates TMEM; lane 0 issues the QK products.
-//   warp 10  lane 0 issues the PV products (one issuing thread could not keep
-//            up: a tcgen05.mma costs its issuer ~80 cycles).
+//   warp 1   allocates TMEM; issues the QK products (one elected lane).
+//   warp 10  issues the PV products (one elected lane).  Two issuing warps,
+//            each converged, keep a tile's 16 MMAs off one instruction stream.
 //   warps 2-9  softmax, two warpgroups: one thread per token of the tile (its
 //            TMEM lane); warps 2-5 take the first half of the query rows,
 //            warps 6-9 the second, each group on its own.
@@ -34,8 +34,9 @@
 //            needs, so every stage carries its own P buffer.
 // fp8 pages: QK runs as kind::f8f6f4 on the e4m3 K codes as they arrive, with
 // Q split into two e4m3 terms (q * 2^e_r = hi + lo, a power-of-two scale per
-// row) accumulated into the same S; each softmax thread converts its token's
-// V row to f16 (exact for e4m3) and PV runs as kind::f16 with f16 P.  The
+// row) accumulated into the same S; V rows are converted to f16 (exact for
+// e4m3), by warps 11-14 as each tile lands when a work item has up to 32 rows,
+// else by the softmax threads one tile ahead, and PV runs as kind::f16 with f16 P.  The
 // scales k_scale and v_scale are folded into the score scale and the output.
 //
 // Every mbarrier wait is bounded (about two seconds); on expiry the CTA sets
@@ -64,7 +65,7 @@ constexpr int kSoftmaxWarp0 = 2;
 constexpr int kSoftmaxGroups = 2;                   // warpgroups splitting the query rows
 constexpr int kSoftmaxWarps = 4 * kSoftmaxGroups;
 constexpr int kPvWarp = kSoftmaxWarp0 + kSoftmaxWarps;   // 10: issues the PV products
-constexpr int kThreads = 32 * (kPvWarp + 1);        // 352
+constexpr int kConvWarp0 = kPvWarp + 1;             // 11-14: fp8 V converters, where present
 constexpr float kRescaleLog2 = 8.0f;
 constexpr long long kWaitLimit = 4000000000LL;      // cycles (~2 s)
 constexpr uint32_t kFull = 0xffffffffu;
@@ -84,6 +85,10 @@ struct Cfg {
     static constexpr int kQBytes = 2 * RP * 128;            // bf16: two 64-column chunks; fp8: hi and lo terms
     static constexpr int kMiscBytes = 4096;
     static constexpr int kRH = RP / kSoftmaxGroups;          // rows per softmax warpgroup
+    // fp8 with up to 32 rows: a warpgroup of its own converts V, leaving the softmax warps
+    // P alone (with 64 rows the softmax needs the registers; it converts V itself)
+    static constexpr bool kConvWarps = FP8 && RP <= 32;
+    static constexpr int kThreads = 32 * (kConvWarp0 + (kConvWarps ? 4 : 0));   // 352 or 480
     static constexpr int kStages = (3 * kStageBytes + kQBytes + kMiscBytes <= kMaxSmem) ? 3 : 2;
     static constexpr int kOffQ = kStages * kStageBytes;
     static constexpr int kOffMisc = kOffQ + kQBytes;
@@ -104,7 +109,8 @@ struct Cfg {
     static constexpr int kBarSFree = kBarSFull + 16;         // [2]
     static constexpr int kBarPFull = kBarSFree + 16;         // [2], by tile parity
     static constexpr int kBarODone = kBarPFull + 16;         // committed once, after the last PV
-    static constexpr int kTmemSlot = kBarODone + 8;
+    static constexpr int kBarVReady = kBarODone + 8;         // [kStages]: V converted (converter warps)
+    static constexpr int kTmemSlot = kBarVReady + 8 * kStages;
     static constexpr int kAbort = kTmemSlot + 4;
     static constexpr int kPvIssued = kAbort + 4;             // int: PVs issued so far (written by the PV thread)
     static constexpr int kFlags = kPvIssued + 4;             // int[group][3][4]: per tile parity, then the epilogue
@@ -217,8 +223,31 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
+// fp8: 16-byte unit u (dims 16u..16u+15) of token tau's V code row in stage `sb`
+// (TMA-swizzled) to f16, written as units 2(u%4), 2(u%4)+1 of the token's row in
+// the MN-major operand atom of dims [64(u/4), 64(u/4)+64); zeros if `zero`.
+template <int kGroupBytes, int kOffV>
+__device__ __forceinline__ void convert_v_unit(uint8_t *sb, int tau, int u, bool zero)
+{
+    const uint8_t *vraw = sb + (tau >> 3) * kGroupBytes + 1024 + (tau & 7) * 128;
+    uint8_t *atom = sb + kOffV + (u >> 2) * kChunkRegion + (tau >> 3) * 1024 + (tau & 7) * 128;
+    uint4 cv = *reinterpret_cast<const uint4 *>(vraw + ((u ^ (tau & 7)) << 4));
+    if (zero)
+        cv = make_uint4(0u, 0u, 0u, 0u);
+    const uint32_t wv[4] = {cv.x, cv.y, cv.z, cv.w};
+    uint32_t hv[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        hv[2 * k] = e4m3x2_to_f16x2(wv[k]);
+        hv[2 * k + 1] = e4m3x2_to_f16x2(wv[k] >> 16);
+    }
+    const int u0 = 2 * (u & 3);
+    *reinterpret_cast<uint4 *>(atom + ((u0 ^ (tau & 7)) << 4)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+    *reinterpret_cast<uint4 *>(atom + (((u0 + 1) ^ (tau & 7)) << 4)) = make_uint4(hv[4], hv[5], hv[6], hv[7]);
+}
+
 template <int RP, bool FP8>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<RP, FP8>::kThreads, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
 {
     using C = Cfg<RP, FP8>;
@@ -255,6 +284,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
     auto bar_pfull = [&](int b) { return mbase + C::kBarPFull + 8 * b; };
     volatile int *pv_issued = reinterpret_cast<volatile int *>(misc + C::kPvIssued);
     const uint32_t bar_odone = mbase + C::kBarODone;
+    auto bar_vready = [&](int s) { return mbase + C::kBarVReady + 8 * s; };
     const uint32_t q_s = sbase + C::kOffQ;
     auto stage = [&](int s) { return sbase + (uint32_t)(s * kStageBytes); };
 
@@ -266,6 +296,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(bar_full(s), 1);
             mbar_init(bar_empty(s), 1);
+            mbar_init(bar_vready(s), 4);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_sfull(b), 1);
@@ -282,7 +313,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
         tmem_relinquish();
     }
     if constexpr (!FP8) {
-        for (int u = threadIdx.x; u < RP * 16; u += kThreads) {
+        for (int u = threadIdx.x; u < RP * 16; u += C::kThreads) {
             const int r = u >> 4, unit = u & 15;
             uint4 val = make_uint4(0u, 0u, 0u, 0u);
             if (r < R) {
@@ -293,12 +324,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             const int chunk = unit >> 3, uu = unit & 7;
             st_shared_v4(q_s + chunk * (RP * 128) + r * 128 + ((uu ^ (r & 7)) << 4), val.x, val.y, val.z, val.w);
         }
-        for (int r = threadIdx.x; r < RP; r += kThreads)
+        for (int r = threadIdx.x; r < RP; r += C::kThreads)
             crow[r] = p.score_scale_log2;
     } else {
         // Row r of Q scaled by 2^e (max |q| lands in [128, 256)), as two e4m3 terms hi + lo.
         // One warp per row; lane l owns dimensions 4l..4l+3.
-        for (int r = warp; r < RP; r += kThreads / 32) {
+        for (int r = warp; r < RP; r += C::kThreads / 32) {
             float qv[4] = {0.f, 0.f, 0.f, 0.f};
             if (r < R) {
                 const int j = r / p.G, i = r - j * p.G;
@@ -339,7 +370,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                 crow[r] = p.score_scale_log2 * ldexpf(1.f, -e);
         }
     }
-    for (int r = threadIdx.x; r < RP; r += kThreads) {
+    for (int r = threadIdx.x; r < RP; r += C::kThreads) {
         m_run[r] = -CUDART_INF_F;
         m_thr[r] = -CUDART_INF_F;
         m_sub[r] = 0.f;
@@ -469,6 +500,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             // stage (empty), which is also how the softmax learns that O holds tile i.
             for (int i = 0; i < ntiles && ok; ++i) {
                 ok = mbar_wait_bounded(bar_pfull(i & 1), (i >> 1) & 1, abort_flag, kWaitLimit);
+                if (C::kConvWarps && ok)   // V(i) in f16; its phase cannot run ahead: tile i+kStages needs PV(i)
+                    ok = mbar_wait_bounded(bar_vready(i % C::kStages), (i / C::kStages) & 1, abort_flag, kWaitLimit);
                 ok = __all_sync(kFull, ok);
                 if (!ok)
                     break;
@@ -496,6 +529,36 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             }
         }
         __syncwarp();
+    } else if (C::kConvWarps && warp >= kConvWarp0) {
+        // ================================================================ fp8 V converters
+        // One thread per token row of the tile: its 128 V codes to f16 in the MN-major operand
+        // layout as soon as the tile lands (rows past L in the last page become zeros), then
+        // the stage's vready barrier tells the PV issuer.  The converted area of a stage is
+        // rewritten only after its next load, which waits for the PV that read it.
+        const int tau = (warp - kConvWarp0) * 32 + lane;
+        const int last_page_end = (w.L + kPage - 1) / kPage * kPage;
+        bool ok = true;
+        for (int j = 0; j < ntiles; ++j) {
+            const int st = j % C::kStages;
+            ok = mbar_wait_bounded(bar_full(st), (j / C::kStages) & 1, abort_flag, kWaitLimit);
+            ok = __all_sync(kFull, ok);
+            if (!ok)
+                break;
+            const int tokv = k0 + j * kTokTile + tau;
+            const bool zero = tokv >= w.L && tokv < last_page_end;
+            uint8_t *sb = smem + st * kStageBytes;
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                convert_v_unit<C::kGroupBytes, C::kOffV>(sb, tau, u, zero);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(bar_vready(st));
+        }
+        if (!ok && lane == 0) {
+            *abort_flag = 1;
+            atomicOr(p.status, SK_DEV_TIMEOUT);
+        }
     } else {
         // ================================================================ softmax warpgroups
         // Group g owns query rows [g*RH, (g+1)*RH): their S and O columns, running max, row
@@ -524,29 +587,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             const bool got = mbar_wait_bounded(bar_full(stv), (jt / C::kStages) & 1, abort_flag, kWaitLimit);
             const int tokv = k0 + jt * kTokTile + tau;
             const bool zero = !got || (tokv >= w.L && tokv < last_page_end);
-            const uint8_t *vraw = smem + stv * kStageBytes + (tau >> 3) * C::kGroupBytes + 1024 + (tau & 7) * 128;
-            uint8_t *atom = smem + stv * kStageBytes + C::kOffV + wg * kChunkRegion + (tau >> 3) * 1024 + (tau & 7) * 128;
 #pragma unroll
-            for (int uu = 0; uu < 4; ++uu) {
-                const int u = 4 * wg + uu;                                                    // dims 16u..16u+15
-                uint4 cv = *reinterpret_cast<const uint4 *>(vraw + ((u ^ (tau & 7)) << 4));
-                if (zero)
-                    cv = make_uint4(0u, 0u, 0u, 0u);
-                const uint32_t wv[4] = {cv.x, cv.y, cv.z, cv.w};
-                uint32_t hv[8];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    hv[2 * k] = e4m3x2_to_f16x2(wv[k]);
-                    hv[2 * k + 1] = e4m3x2_to_f16x2(wv[k] >> 16);
-                }
-                // f16 dims 16u..16u+7 and 16u+8..16u+15: units 2 uu and 2 uu + 1 of the atom row
-                const int u0 = 2 * uu;
-                *reinterpret_cast<uint4 *>(atom + ((u0 ^ (tau & 7)) << 4)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-                *reinterpret_cast<uint4 *>(atom + (((u0 + 1) ^ (tau & 7)) << 4)) = make_uint4(hv[4], hv[5], hv[6], hv[7]);
-            }
+            for (int uu = 0; uu < 4; ++uu)
+                convert_v_unit<C::kGroupBytes, C::kOffV>(smem + stv * kStageBytes, tau, 4 * wg + uu, zero);
             return got;
         };
-        if constexpr (FP8) {
+        if constexpr (FP8 && !C::kConvWarps) {
             if (ntiles > 0 && !convert_v(0))
                 failed = true;
         }
@@ -703,7 +749,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                 mbar_arrive(bar_pfull(b));
             // fp8: the next tile's V conversion fills the wait for its S (its stage is free once it
             // has landed); the fence before that tile's P_full publishes it to the tensor core
-            if (FP8 && !failed && j + 1 < ntiles && !convert_v(j + 1))
+            if (FP8 && !C::kConvWarps && !failed && j + 1 < ntiles && !convert_v(j + 1))
                 failed = true;
             if (failed) {
                 // the next tile's group decision propagates the failure
@@ -812,7 +858,7 @@ cudaError_t launch_rp(const CUtensorMap &map, const AttnParams &p, cudaStream_t 
     if (attr_err != cudaSuccess)
         return attr_err;
     const dim3 grid((unsigned)p.num_items * (unsigned)p.H_kv);
-    attn_tc_kernel<RP, FP8><<<grid, kThreads, Cfg<RP, FP8>::kSmemBytes, stream>>>(map, p);
+    attn_tc_kernel<RP, FP8><<<grid, Cfg<RP, FP8>::kThreads, Cfg<RP, FP8>::kSmemBytes, stream>>>(map, p);
     return cudaGetLastError();
 }
 

@@ -34,11 +34,13 @@ def _small_problems():
         build_problem([4000], 4, 32, 2, seed=27),                # bs 1: long single sequence
         build_problem([130, 70], 8, 128, 8, seed=28),            # 128 rows per work item (G16 x q8)
         build_problem([300, 20], 2, 40, 4, seed=29),             # G = 10, rows not a power of two
+        build_problem([700, 130, 2000, 9], [4, 4, 3, 4], 32, 2, kv_dtype=KV_FP8, k_scale=0.5, v_scale=0.25,
+                      seed=30),                                  # fp8 with 64 rows per work item
     ]
 
 
 @pytest.mark.parametrize("use_plan", [True, False])
-@pytest.mark.parametrize("k", range(9))
+@pytest.mark.parametrize("k", range(10))
 def test_small_problem_elementwise(k, use_plan):
     pr = _small_problems()[k]
     q, kv = problem_tensors(pr, DEV)
@@ -56,7 +58,7 @@ def test_small_problem_elementwise(k, use_plan):
     assert np.max(np.abs(lse[fin] - ref_lse[fin]), initial=0) <= 1e-3
 
 
-@pytest.mark.parametrize("k", [0, 2, 3, 6])
+@pytest.mark.parametrize("k", [0, 2, 3, 6, 9])
 def test_small_problem_partials(k):
     """Every segment partial: o / l and m + log l are the segment's unique output
     and log-sum-exp; a row that sees no key of the segment has (-inf, 0, 0)."""
@@ -183,7 +185,7 @@ def test_repeated_calls_are_bit_identical_under_perturbed_timing():
     returns bit-identical outputs (a missed wait shows up here as a flaky row)."""
     d = torch.device(DEV)
     noise = torch.randn((2048, 2048), device=d)
-    for pr in (_small_problems()[0], _small_problems()[6], _small_problems()[8]):
+    for pr in (_small_problems()[0], _small_problems()[3], _small_problems()[6], _small_problems()[8], _small_problems()[9]):
         q, kv = problem_tensors(pr, DEV)
         ref, _ = oracle_problem(pr)
         first = None
