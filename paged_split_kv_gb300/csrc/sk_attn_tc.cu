@@ -308,12 +308,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
         *pv_issued = 0;
         fence_mbar_init();
     }
+    __syncthreads();   // barriers initialised: the producer starts its copies now
+    // The other warps set up TMEM and Q meanwhile, then meet at a barrier of their own.
+    constexpr uint32_t kSetupBar = 3;
+    constexpr int kSetupThreads = C::kThreads - 32;
+    const int st_tid = threadIdx.x - 32;
+    if (warp != 0) {
     if (warp == 1) {
         tmem_alloc(mbase + C::kTmemSlot, C::kTmemCols);
         tmem_relinquish();
     }
     if constexpr (!FP8) {
-        for (int u = threadIdx.x; u < RP * 16; u += C::kThreads) {
+        for (int u = st_tid; u < RP * 16; u += kSetupThreads) {
             const int r = u >> 4, unit = u & 15;
             uint4 val = make_uint4(0u, 0u, 0u, 0u);
             if (r < R) {
@@ -324,12 +330,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             const int chunk = unit >> 3, uu = unit & 7;
             st_shared_v4(q_s + chunk * (RP * 128) + r * 128 + ((uu ^ (r & 7)) << 4), val.x, val.y, val.z, val.w);
         }
-        for (int r = threadIdx.x; r < RP; r += C::kThreads)
+        for (int r = st_tid; r < RP; r += kSetupThreads)
             crow[r] = p.score_scale_log2;
     } else {
         // Row r of Q scaled by 2^e (max |q| lands in [128, 256)), as two e4m3 terms hi + lo.
         // One warp per row; lane l owns dimensions 4l..4l+3.
-        for (int r = warp; r < RP; r += C::kThreads / 32) {
+        for (int r = warp - 1; r < RP; r += kSetupThreads / 32) {
             float qv[4] = {0.f, 0.f, 0.f, 0.f};
             if (r < R) {
                 const int j = r / p.G, i = r - j * p.G;
@@ -370,16 +376,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                 crow[r] = p.score_scale_log2 * ldexpf(1.f, -e);
         }
     }
-    for (int r = threadIdx.x; r < RP; r += C::kThreads) {
+    for (int r = st_tid; r < RP; r += kSetupThreads) {
         m_run[r] = -CUDART_INF_F;
         m_thr[r] = -CUDART_INF_F;
         m_sub[r] = 0.f;
     }
     fence_proxy_async_smem();
     tc_fence_before();
-    __syncthreads();
+    named_bar_sync(kSetupBar, kSetupThreads);
     tc_fence_after();
-    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(misc + C::kTmemSlot);
+    }
+    const uint32_t tmem = warp != 0 ? *reinterpret_cast<volatile uint32_t *>(misc + C::kTmemSlot) : 0u;
     const uint32_t tmem_s0 = tmem, tmem_o = tmem + 2 * RP;
 
     if (warp == 0) {
@@ -787,9 +794,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             alpha_s[r0 + tid] = (gred[tid] + gred[32 + tid]) + (gred[64 + tid] + gred[96 + tid]);
         named_bar_sync(bar_id, 128);
         if (write) {
+            // O^T of the group's rows -> stage 0 as [row][128] fp32 (every copy and MMA is done:
+            // the stages are free), then one 512-byte bulk store per row into the partials
             if (ntiles > 0)
                 tc_fence_after();
-            const long long seg_base = (long long)w.g * p.H_q + h * p.G;
+            float *orow = reinterpret_cast<float *>(smem);
 #pragma unroll
             for (int c = 0; c < RH; c += kLd) {
                 float o[kLd];
@@ -804,17 +813,21 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
 #pragma unroll
                 for (int rr = 0; rr < kLd; ++rr) {
                     const int r = r0 + c + rr;
-                    if (r < R) {
-                        const int jq = r / p.G, i = r - jq * p.G;
-                        const long long slot = (long long)(w.tok0 + jq) * p.seg_max * p.H_q + seg_base + i;
-                        const float l = alpha_s[r];
-                        p.part_o[slot * kHeadDim + tau] = l > 0.f ? o[rr] * p.v_scale : 0.f;
-                        if (tau == 0) {
-                            p.part_m[slot] = l > 0.f ? m_run[r] * 0.69314718055994531f : -CUDART_INF_F;
-                            p.part_l[slot] = l;
-                        }
-                    }
+                    orow[r * kHeadDim + tau] = alpha_s[r] > 0.f ? o[rr] * p.v_scale : 0.f;
                 }
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(bar_id, 128);
+            const int r = r0 + tid;
+            if (tid < RH && r < R) {
+                const int jq = r / p.G, i = r - jq * p.G;
+                const long long slot = (long long)(w.tok0 + jq) * p.seg_max * p.H_q + (long long)w.g * p.H_q + h * p.G + i;
+                bulk_store_s2g(p.part_o + slot * kHeadDim, sbase + (uint32_t)(r * kHeadDim * 4), kHeadDim * 4);
+                bulk_commit_group();
+                const float l = alpha_s[r];
+                p.part_m[slot] = l > 0.f ? m_run[r] * 0.69314718055994531f : -CUDART_INF_F;
+                p.part_l[slot] = l;
+                bulk_wait_reads();
             }
         }
     }

@@ -2,12 +2,18 @@
 // gfx950 assembly attention: length-aware split-KV for dynamic workload",
 // Modifications, first item).
 //
-// One CTA of 1024 threads does the whole batch (bs <= 32767), entirely on the
-// device, so the call never reads anything back and can be captured in a
-// CUDA graph.  The page's rule -- the smallest T with total segments <= B and
-// per-sequence segments <= seg_max -- is monotone in T (both counts only fall
-// as T grows), so T is found by binary search over [1, max tiles] instead of
-// trying every T; each probe is one block-wide sum.
+// One CTA does the whole batch (bs <= 32767), entirely on the device, so the
+// call never reads anything back and can be captured in a CUDA graph.  The
+// page's rule -- the smallest T with total segments <= B and per-sequence
+// segments <= seg_max -- is monotone in T (both counts only fall as T grows),
+// so T is found by binary search instead of trying every T.  The search runs
+// between two bounds that follow from ceil(x) in [x, x + 1): with S tiles in
+// n non-empty sequences, no T < S / B fits (the total is at least S / T), and
+// every T >= S / (B - n) does (the total is below S / T + n).
+//
+// The CTA has one warp per 32 sequences (at most 1024 threads); tile counts
+// sit in shared memory for batches up to kCacheSeqs, so a probe is one pass
+// over them and one barrier (partial sums double-buffered by probe parity).
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -16,77 +22,69 @@
 namespace sk {
 namespace {
 
-constexpr int kPlanThreads = 1024;
-constexpr int kWarps = kPlanThreads / 32;
-
-__device__ long long block_sum(long long v, long long *scratch)
-{
-    for (int o = 16; o > 0; o >>= 1)
-        v += __shfl_xor_sync(0xffffffffu, v, o);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    __syncthreads();
-    if (lane == 0)
-        scratch[warp] = v;
-    __syncthreads();
-    long long r = 0;
-    if (warp == 0) {
-        r = lane < kWarps ? scratch[lane] : 0;
-        for (int o = 16; o > 0; o >>= 1)
-            r += __shfl_xor_sync(0xffffffffu, r, o);
-        if (lane == 0)
-            scratch[kWarps] = r;
-    }
-    __syncthreads();
-    return scratch[kWarps];
-}
-
-__device__ long long block_max(long long v, long long *scratch)
-{
-    for (int o = 16; o > 0; o >>= 1) {
-        long long w = __shfl_xor_sync(0xffffffffu, v, o);
-        v = w > v ? w : v;
-    }
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    __syncthreads();
-    if (lane == 0)
-        scratch[warp] = v;
-    __syncthreads();
-    if (warp == 0) {
-        long long r = lane < kWarps ? scratch[lane] : 0;
-        for (int o = 16; o > 0; o >>= 1) {
-            long long w = __shfl_xor_sync(0xffffffffu, r, o);
-            r = w > r ? w : r;
-        }
-        if (lane == 0)
-            scratch[kWarps] = r;
-    }
-    __syncthreads();
-    return scratch[kWarps];
-}
+constexpr int kPlanMaxThreads = 1024;
+constexpr int kCacheSeqs = 8192;
+constexpr uint32_t kFull = 0xffffffffu;
 
 __device__ __forceinline__ long long tiles_of(int L)
 {
     return L > 0 ? ((long long)L + kTile - 1) / kTile : 0;
 }
 
-__global__ void __launch_bounds__(kPlanThreads, 1)
+__device__ __forceinline__ long long warp_sum(long long v)
+{
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(kFull, v, o);
+    return v;
+}
+
+__device__ __forceinline__ long long warp_max(long long v)
+{
+    for (int o = 16; o > 0; o >>= 1) {
+        const long long w = __shfl_xor_sync(kFull, v, o);
+        v = w > v ? w : v;
+    }
+    return v;
+}
+
+__global__ void __launch_bounds__(kPlanMaxThreads, 1)
 plan_kernel(const int32_t *__restrict__ seq_lens, const int32_t *__restrict__ cu_q, int bs,
             int num_tokens, int budget, int seg_max, int32_t *__restrict__ plan, int plan_capacity,
             int32_t *__restrict__ tok_nseg, int *status)
 {
-    __shared__ long long red[kWarps + 1];
-    __shared__ long long scan[kPlanThreads];
-    const int tid = threadIdx.x;
+    __shared__ int32_t tiles_s[kCacheSeqs];
+    __shared__ long long part[2][32];
+    __shared__ long long part3[3][32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nthr = blockDim.x, nwarps = nthr >> 5;
+    const bool cached = bs <= kCacheSeqs;
+    auto tiles_at = [&](int s) -> long long { return cached ? (long long)tiles_s[s] : tiles_of(__ldg(seq_lens + s)); };
 
-    // 1. largest tile count and number of non-empty sequences
-    long long my_max = 0, my_nonempty = 0;
-    for (int s = tid; s < bs; s += kPlanThreads) {
+    // 1. tile counts; largest, number of non-empty sequences, total
+    long long my_max = 0, my_nonempty = 0, my_sum = 0;
+    for (int s = tid; s < bs; s += nthr) {
         const long long t = tiles_of(__ldg(seq_lens + s));
+        if (cached)
+            tiles_s[s] = (int32_t)t;              // < 2^26: lengths are int32
         my_max = t > my_max ? t : my_max;
         my_nonempty += t > 0;
+        my_sum += t;
     }
-    const long long max_tiles = block_max(my_max, red);
-    const long long nonempty = block_sum(my_nonempty, red);
+    my_max = warp_max(my_max);
+    my_nonempty = warp_sum(my_nonempty);
+    my_sum = warp_sum(my_sum);
+    if (lane == 0) {
+        part3[0][warp] = my_max;
+        part3[1][warp] = my_nonempty;
+        part3[2][warp] = my_sum;
+    }
+    __syncthreads();
+    long long max_tiles = 0, nonempty = 0, total_tiles = 0;
+    for (int k = 0; k < nwarps; ++k) {
+        max_tiles = part3[0][k] > max_tiles ? part3[0][k] : max_tiles;
+        nonempty += part3[1][k];
+        total_tiles += part3[2][k];
+    }
 
     // 2. T: the smallest feasible t, or one segment per non-empty sequence
     long long T;
@@ -94,18 +92,34 @@ plan_kernel(const int32_t *__restrict__ seq_lens, const int32_t *__restrict__ cu
     if (nonempty > budget) {
         T = hi_all;
     } else {
-        // t = hi_all is feasible (total = nonempty <= budget, per-sequence 1 <= seg_max).
-        long long lo = 1, hi = hi_all;
-        const long long per_seq_lo = (max_tiles + seg_max - 1) / seg_max;
-        lo = per_seq_lo > lo ? per_seq_lo : lo;
+        // t = hi_all is feasible (total = nonempty <= budget, per-sequence 1 <= seg_max)
+        long long lo = (max_tiles + seg_max - 1) / seg_max;
+        const long long by_total = budget > 0 ? (total_tiles + budget - 1) / budget : 0;
+        lo = by_total > lo ? by_total : lo;
+        lo = lo < 1 ? 1 : lo;
+        long long hi = hi_all;
+        if (budget > nonempty) {
+            const long long fits = (total_tiles + (budget - nonempty) - 1) / (budget - nonempty);
+            const long long h2 = fits > lo ? fits : lo;
+            hi = h2 < hi ? h2 : hi;
+        }
         if (lo > hi)
             lo = hi;
+        int parity = 0;
         while (lo < hi) {
             const long long mid = lo + (hi - lo) / 2;
-            long long part = 0;
-            for (int s = tid; s < bs; s += kPlanThreads)
-                part += (tiles_of(__ldg(seq_lens + s)) + mid - 1) / mid;
-            const long long total = block_sum(part, red);
+            const uint32_t m32 = (uint32_t)mid;   // tile counts and mid are below 2^26
+            long long sum = 0;
+            for (int s = tid; s < bs; s += nthr)
+                sum += ((uint32_t)tiles_at(s) + m32 - 1u) / m32;
+            sum = warp_sum(sum);
+            if (lane == 0)
+                part[parity][warp] = sum;
+            __syncthreads();
+            long long total = 0;
+            for (int k = 0; k < nwarps; ++k)
+                total += part[parity][k];
+            parity ^= 1;
             const bool ok = total <= budget && (max_tiles + mid - 1) / mid <= seg_max;
             if (ok)
                 hi = mid;
@@ -115,29 +129,35 @@ plan_kernel(const int32_t *__restrict__ seq_lens, const int32_t *__restrict__ cu
         T = lo;
     }
 
-    // 3. exclusive prefix sum of nseg_s over a contiguous chunk per thread
-    const int chunk = (bs + kPlanThreads - 1) / kPlanThreads;
+    // 3. exclusive prefix sum of nseg_s over a contiguous chunk of sequences per thread
+    const int chunk = (bs + nthr - 1) / nthr;
     const int s_begin = tid * chunk;
     const int s_end = min(bs, s_begin + chunk);
     long long mine = 0;
     for (int s = s_begin; s < s_end; ++s)
-        mine += (tiles_of(__ldg(seq_lens + s)) + T - 1) / T;
-    scan[tid] = mine;
-    __syncthreads();
-    for (int off = 1; off < kPlanThreads; off <<= 1) {
-        const long long add = tid >= off ? scan[tid - off] : 0;
-        __syncthreads();
-        scan[tid] += add;
-        __syncthreads();
+        mine += (tiles_at(s) + T - 1) / T;
+    long long incl = mine;
+    for (int o = 1; o < 32; o <<= 1) {
+        const long long v = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o)
+            incl += v;
     }
-    long long base = scan[tid] - mine;
-    const long long total_items = scan[kPlanThreads - 1];
+    __syncthreads();                       // every probe has read its partials
+    if (lane == 31)
+        part[0][warp] = incl;
+    __syncthreads();
+    long long base = incl - mine, total_items = 0;
+    for (int k = 0; k < nwarps; ++k) {
+        const long long v = part[0][k];
+        base += k < warp ? v : 0;
+        total_items += v;
+    }
 
     // 4. work list, -1 tail, per-token counts
     if (tid == 0)
         plan[0] = (int32_t)T;
     for (int s = s_begin; s < s_end; ++s) {
-        const int n = (int)((tiles_of(__ldg(seq_lens + s)) + T - 1) / T);
+        const int n = (int)((tiles_at(s) + T - 1) / T);
         for (int g = 0; g < n; ++g) {
             const long long slot = 1 + base + g;
             if (slot < plan_capacity)
@@ -154,7 +174,7 @@ plan_kernel(const int32_t *__restrict__ seq_lens, const int32_t *__restrict__ cu
     }
     if (1 + total_items > plan_capacity && tid == 0)
         atomicOr(status, SK_DEV_BAD_SEQ);
-    for (long long k = 1 + total_items + tid; k < plan_capacity; k += kPlanThreads)
+    for (long long k = 1 + total_items + tid; k < plan_capacity; k += nthr)
         plan[k] = -1;
 }
 
@@ -164,8 +184,10 @@ cudaError_t launch_plan(const int32_t *seq_lens, const int32_t *cu_q, int bs, in
                         int budget, int seg_max, int32_t *plan, int plan_capacity,
                         int32_t *tok_nseg, int *status, cudaStream_t stream)
 {
-    plan_kernel<<<1, kPlanThreads, 0, stream>>>(seq_lens, cu_q, bs, num_tokens, budget, seg_max,
-                                                plan, plan_capacity, tok_nseg, status);
+    const int warps = (bs + 31) / 32;
+    const int threads = 32 * (warps < 1 ? 1 : warps > kPlanMaxThreads / 32 ? kPlanMaxThreads / 32 : warps);
+    plan_kernel<<<1, threads, 0, stream>>>(seq_lens, cu_q, bs, num_tokens, budget, seg_max, plan,
+                                           plan_capacity, tok_nseg, status);
     return cudaGetLastError();
 }
 

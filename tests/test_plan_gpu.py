@@ -73,3 +73,15 @@ def test_plan_capacity_above_minimum_is_padded_with_minus_one():
     plan, tok, cu, cap = _gpu_plan(lens, [4, 4, 4], 2, 148, 64, cap=300)
     ref, _, _, _ = oracle.plan(lens, cu, 2, 148, 64, sk.sk_tile_tokens(), 300)
     np.testing.assert_array_equal(plan, ref)
+
+
+def test_plan_degenerate_budgets_and_batches():
+    """Fewer SMs than KV heads (a budget of 0 work items), an all-empty batch,
+    a single sequence, and a batch at the shared-memory cache edge."""
+    rng = np.random.default_rng(5)
+    _check(np.array([900, 0, 77], np.int32), [1, 1, 1], 8, 4, 64)        # budget 0
+    _check(np.array([0, 0, 0, 0], np.int32), [1, 0, 2, 1], 2, 148, 64)   # nothing to attend
+    _check(np.array([123457], np.int32), [4], 2, 148, 64)                # bs 1
+    for bs in (8192, 8193):
+        lens = rng.integers(0, 50_000, size=bs).astype(np.int32)
+        _check(lens, rng.integers(0, 3, size=bs).astype(np.int32), 2, 152, 64)
