@@ -38,6 +38,13 @@ __device__ __forceinline__ long long warp_sum(long long v)
     return v;
 }
 
+__device__ __forceinline__ uint32_t warp_sum32(uint32_t v)
+{
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(kFull, v, o);
+    return v;
+}
+
 __device__ __forceinline__ long long warp_max(long long v)
 {
     for (int o = 16; o > 0; o >>= 1) {
@@ -54,11 +61,15 @@ plan_kernel(const int32_t *__restrict__ seq_lens, const int32_t *__restrict__ cu
 {
     __shared__ int32_t tiles_s[kCacheSeqs];
     __shared__ long long part[2][32];
+    __shared__ uint32_t part32[2][32];
     __shared__ long long part3[3][32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nthr = blockDim.x, nwarps = nthr >> 5;
     const bool cached = bs <= kCacheSeqs;
-    auto tiles_at = [&](int s) -> long long { return cached ? (long long)tiles_s[s] : tiles_of(__ldg(seq_lens + s)); };
+    // tile counts are below 2^26 (lengths are int32), so they and T fit in 32 bits
+    auto tiles_at = [&](int s) -> uint32_t {
+        return cached ? (uint32_t)tiles_s[s] : (uint32_t)tiles_of(__ldg(seq_lens + s));
+    };
 
     // 1. tile counts; largest, number of non-empty sequences, total
     long long my_max = 0, my_nonempty = 0, my_sum = 0;
@@ -105,22 +116,25 @@ plan_kernel(const int32_t *__restrict__ seq_lens, const int32_t *__restrict__ cu
         }
         if (lo > hi)
             lo = hi;
+        // Every probe has mid >= S / B, so its total is below S / mid + bs <= B + bs < 2^32
+        // (B < 2^31: plan_capacity > B is an int; bs < 2^15).
+        // ceil(max / mid) <= seg_max is max <= seg_max * mid.
         int parity = 0;
         while (lo < hi) {
             const long long mid = lo + (hi - lo) / 2;
-            const uint32_t m32 = (uint32_t)mid;   // tile counts and mid are below 2^26
-            long long sum = 0;
+            const uint32_t m32 = (uint32_t)mid;
+            uint32_t sum = 0;
             for (int s = tid; s < bs; s += nthr)
-                sum += ((uint32_t)tiles_at(s) + m32 - 1u) / m32;
-            sum = warp_sum(sum);
+                sum += (tiles_at(s) + m32 - 1u) / m32;
+            sum = warp_sum32(sum);
             if (lane == 0)
-                part[parity][warp] = sum;
+                part32[parity][warp] = sum;
             __syncthreads();
             long long total = 0;
             for (int k = 0; k < nwarps; ++k)
-                total += part[parity][k];
+                total += part32[parity][k];
             parity ^= 1;
-            const bool ok = total <= budget && (max_tiles + mid - 1) / mid <= seg_max;
+            const bool ok = total <= budget && max_tiles <= (long long)seg_max * mid;
             if (ok)
                 hi = mid;
             else
@@ -133,9 +147,10 @@ plan_kernel(const int32_t *__restrict__ seq_lens, const int32_t *__restrict__ cu
     const int chunk = (bs + nthr - 1) / nthr;
     const int s_begin = tid * chunk;
     const int s_end = min(bs, s_begin + chunk);
+    const uint32_t T32 = (uint32_t)T;
     long long mine = 0;
     for (int s = s_begin; s < s_end; ++s)
-        mine += (tiles_at(s) + T - 1) / T;
+        mine += (tiles_at(s) + T32 - 1u) / T32;
     long long incl = mine;
     for (int o = 1; o < 32; o <<= 1) {
         const long long v = __shfl_up_sync(kFull, incl, o);
@@ -157,7 +172,7 @@ plan_kernel(const int32_t *__restrict__ seq_lens, const int32_t *__restrict__ cu
     if (tid == 0)
         plan[0] = (int32_t)T;
     for (int s = s_begin; s < s_end; ++s) {
-        const int n = (int)((tiles_at(s) + T - 1) / T);
+        const int n = (int)((tiles_at(s) + T32 - 1u) / T32);
         for (int g = 0; g < n; ++g) {
             const long long slot = 1 + base + g;
             if (slot < plan_capacity)
