@@ -12,7 +12,10 @@ they follow.
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 (values the pages print, closed forms, invariants, a library softmax on tiny
-inputs, brute force); none is marked "parity unpinned".
+inputs, brute force) and, for the KV write step and the e4m3fn encoder, by
+``tests/test_kv_write_pins.py`` (round trips through the pinned decoder, IEEE
+midpoints, PyTorch's float8 cast, a hand-written page image, attention on
+directly built pages); none is marked "parity unpinned".
 """
 from __future__ import annotations
 
@@ -56,6 +59,11 @@ def _load():
         lib = ctypes.CDLL(build())
         P = ctypes.c_void_p
         i32, i64, f64 = ctypes.c_int, ctypes.c_int64, ctypes.c_double
+        lib.sko_e4m3fn_encode.restype = ctypes.c_uint8
+        lib.sko_e4m3fn_encode.argtypes = [ctypes.c_float]
+        lib.sko_reshape_and_cache.restype = None
+        lib.sko_reshape_and_cache.argtypes = [P, P, P, i32, i32, i32, P, i32, ctypes.c_float, ctypes.c_float,
+                                              i64, i32]
         lib.sko_bf16_to_double.restype = f64
         lib.sko_bf16_to_double.argtypes = [ctypes.c_uint16]
         lib.sko_e4m3fn_to_double.restype = f64
@@ -96,6 +104,30 @@ def bf16_to_double(bits: int) -> float:
 
 def e4m3fn_to_double(code: int) -> float:
     return _load().sko_e4m3fn_to_double(int(code) & 0xFF)
+
+
+def e4m3fn_encode(x) -> np.ndarray:
+    """e4m3fn codes of binary32 values (nearest, ties to even, saturating)."""
+    x = np.asarray(x, dtype=np.float32)
+    f = _load().sko_e4m3fn_encode
+    return np.array([f(float(v)) for v in x.ravel()], dtype=np.uint8).reshape(x.shape)
+
+
+def reshape_and_cache(key_bits, value_bits, slot_mapping, kv_pages: np.ndarray, kv_dtype: int,
+                      k_scale: float = 1.0, v_scale: float = 1.0) -> np.ndarray:
+    """Writes the tokens' K/V rows into ``kv_pages`` ([NB, H_kv, page, 2D]; uint16
+    bf16 bits or uint8 e4m3 codes) in place and returns it."""
+    key_bits = _c(key_bits, np.uint16)
+    value_bits = _c(value_bits, np.uint16)
+    slot_mapping = _c(slot_mapping, np.int64)
+    nt, hkv, d = key_bits.shape
+    assert value_bits.shape == key_bits.shape and slot_mapping.shape == (nt,)
+    nb, hkv2, page, d2 = kv_pages.shape
+    assert hkv2 == hkv and d2 == 2 * d and kv_pages.flags.c_contiguous
+    assert kv_pages.dtype == (np.uint16 if kv_dtype == KV_BF16 else np.uint8)
+    _load().sko_reshape_and_cache(_ptr(key_bits), _ptr(value_bits), _ptr(slot_mapping), nt, hkv, d,
+                                  _ptr(kv_pages), int(kv_dtype), float(k_scale), float(v_scale), nb, page)
+    return kv_pages
 
 
 def fixed_nseg(bs: int, num_kv_heads: int, num_sms: int, seg_max: int = 64) -> int:

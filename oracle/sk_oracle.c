@@ -64,6 +64,32 @@ double sko_e4m3fn_to_double(uint8_t code)
     return sign ? -mag : mag;
 }
 
+/* The e4m3fn code nearest to the binary32 value x, by the same format
+ * definition: scan the 127 non-negative finite codes (decoded above) for the
+ * closest magnitude, ties going to the even code (even mantissa, as in
+ * round-to-nearest-even).  Magnitudes of 448 and above saturate to 448 (0x7E),
+ * infinities included; NaN gives 0x7F.  The sign is kept, so -0 and negative
+ * values that round to zero give 0x80. */
+uint8_t sko_e4m3fn_encode(float x)
+{
+    if (isnan(x))
+        return 0x7F;
+    const int neg = signbit(x) != 0;
+    const double a = fabs((double)x);
+    int best = 0x7E;
+    if (a < 448.0) {
+        double best_d = INFINITY;
+        for (int c = 0; c <= 0x7E; ++c) {
+            const double d = fabs(sko_e4m3fn_to_double((uint8_t)c) - a);
+            if (d < best_d || (d == best_d && (c & 1) == 0)) {
+                best_d = d;
+                best = c;
+            }
+        }
+    }
+    return (uint8_t)(best | (neg ? 0x80 : 0));
+}
+
 static int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 /* ---------------------------------------------------------------------------
@@ -413,6 +439,50 @@ void sko_merge(const float *part_o, const float *part_m, const float *part_l,
         }
         if (lse)
             lse[i] = Lam > 0.0 ? M + log(Lam) : -INFINITY;
+    }
+}
+
+/* ---------------------------------------------------------------------------
+ * [RFC] Background: the KV write of the backends that keep standard pages.
+ * Token t's K and V rows for KV head h land side by side in row
+ * (slot % page) of block (slot / page), slot = slot_mapping[t]:
+ *   pages[blk][h][off][0:D] = K[t][h][:],  pages[blk][h][off][D:2D] = V[t][h][:].
+ * A negative slot marks a token without a cache slot: nothing is written for
+ * it, nor for a slot past the last block.  Tokens are taken in order, so a
+ * slot given twice ends with the later token (the GPU path leaves that case
+ * undefined).  bf16 pages receive the input bits unchanged; e4m3 pages
+ * receive sko_e4m3fn_encode(x / scale), the quotient rounded to binary32
+ * (IEEE division, the precision the CUDA path divides in), with k_scale for
+ * K and v_scale for V. */
+void sko_reshape_and_cache(const uint16_t *key, const uint16_t *value, const int64_t *slot_mapping,
+                           int num_tokens, int num_kv_heads, int head_dim, void *kv_pages,
+                           int kv_dtype, float k_scale, float v_scale, int64_t num_blocks, int page)
+{
+    const int64_t row_elems = 2 * (int64_t)head_dim;
+    for (int t = 0; t < num_tokens; ++t) {
+        const int64_t slot = slot_mapping[t];
+        if (slot < 0)
+            continue;
+        const int64_t blk = slot / page, off = slot % page;
+        if (blk >= num_blocks)
+            continue;
+        for (int h = 0; h < num_kv_heads; ++h) {
+            const int64_t row = ((blk * num_kv_heads + h) * page + off) * row_elems;
+            const int64_t src = ((int64_t)t * num_kv_heads + h) * head_dim;
+            for (int d = 0; d < head_dim; ++d) {
+                if (kv_dtype == SKO_KV_BF16) {
+                    uint16_t *pg = (uint16_t *)kv_pages;
+                    pg[row + d] = key[src + d];
+                    pg[row + head_dim + d] = value[src + d];
+                } else {
+                    uint8_t *pg = (uint8_t *)kv_pages;
+                    const float kq = (float)sko_bf16_to_double(key[src + d]) / k_scale;
+                    const float vq = (float)sko_bf16_to_double(value[src + d]) / v_scale;
+                    pg[row + d] = sko_e4m3fn_encode(kq);
+                    pg[row + head_dim + d] = sko_e4m3fn_encode(vq);
+                }
+            }
+        }
     }
 }
 
