@@ -54,6 +54,8 @@ def _args():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kv-write", choices=["bf16", "fp8"], default=None,
+                    help="time the KV write step (65536 tokens x 8 KV heads) instead of the path")
     ap.add_argument("--fixed-split", action="store_true",
                     help="time the fixed split even when bs > 1 (bs == 1 always uses it, as the method does)")
     return ap.parse_args()
@@ -479,8 +481,62 @@ def run_sk(a, w, ws, rank, local):
     return 0
 
 
+def run_kv_write(a, local):
+    """The KV write step on a prefill-sized chunk: 65536 new tokens x 8 KV heads
+    scattered into shuffled page rows (256 MB of bf16 K/V in, larger than L2)."""
+    import torch
+    import paged_split_kv_gb300 as sk
+    if not os.path.exists(sk.LIB_PATH):
+        from paged_split_kv_gb300 import build as b
+        b.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    nt, hkv, d, page = 65536, 8, 128, 16
+    fp8 = a.kv_write == "fp8"
+    g = torch.Generator(device=dev).manual_seed(77)
+    key = torch.randn((nt, hkv, d), generator=g, device=dev).to(torch.bfloat16)
+    val = torch.randn((nt, hkv, d), generator=g, device=dev).to(torch.bfloat16)
+    nb = nt // page + 64
+    slots = torch.randperm(nb * page, generator=g, device=dev)[:nt].to(torch.int64)
+    pages = torch.empty((nb, hkv, page, 2 * d), dtype=torch.uint8 if fp8 else torch.bfloat16, device=dev)
+    ks, vs = (0.5, 0.25) if fp8 else (1.0, 1.0)
+    f = lambda: sk.sk_reshape_and_cache(key, val, slots, pages, k_scale=ks, v_scale=vs)
+    for _ in range(max(3, a.warmup)):
+        f()
+    torch.cuda.synchronize()
+    if sk.sk_get_device_status(clear=True):
+        raise RuntimeError("device status set by the KV write")
+    sampler = ClockSampler(local)
+    sampler.start()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.steps)]
+    torch.cuda.synchronize()
+    for e0, e1 in evs:
+        e0.record()
+        f()
+        e1.record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
+    moved = nt * hkv * (2 * d * 2 + 2 * d * (1 if fp8 else 2)) + nt * 8   # K/V in, page rows out, slots
+    gbs = moved / (ms * 1e-3) / 1e9
+    peak, kind = _peaks()
+    line = {"metric": "KV write GB/s (reshape_and_cache into standard pages)", "value": round(gbs, 1),
+            "unit": "GB/s", "n_gpus": 1, "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(ms, 5),
+            "higher_is_better": True, "dtype": "fp8_e4m3" if fp8 else "bf16", "data": "synthetic",
+            "config": {"workload": f"kv_write_{nt}x{hkv}_{a.kv_write}", "tokens": nt, "num_kv_heads": hkv,
+                       "head_dim": d, "page": page, "l2": "inputs larger than L2, no flush"},
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(gbs / peak, 4), "peak_kind": kind, "traffic": None,
+                         "algorithmic_bytes_per_launch": int(moved)},
+            "clocks": clocks, "gpu_launches": a.steps}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     a = _args()
+    if a.kv_write:
+        return run_kv_write(a, int(os.environ.get("LOCAL_RANK", 0)))
     ws, rank, local = _dist()
     w = si.config(a.config)
     if a.impl == "reference":

@@ -181,6 +181,34 @@ int sk_merge_segments(const float *part_o, const float *part_m, const float *par
                       const int32_t *tok_nseg, int fixed_nseg, int num_tokens, int num_q_heads,
                       int head_dim, int seg_max, void *out, float *lse, void *stream);
 
+/* KV write: store this step's K and V rows into standard pages through a
+ * slot mapping (the writer of the backends that keep standard pages, vLLM RFC
+ * 59111, Background: per head, a token row holds K and V side by side).
+ *
+ * For token t and KV head h with slot = slot_mapping[t] >= 0:
+ *   kv_pages[slot / page_size][h][slot % page_size][0 : D)  = K[t][h][:]
+ *   kv_pages[slot / page_size][h][slot % page_size][D : 2D) = V[t][h][:]
+ * bf16 pages receive the input bits unchanged.  e4m3fn pages
+ * (kv_dtype == SK_KV_FP8_E4M3) receive each value divided by k_scale (K) or
+ * v_scale (V) in IEEE binary32 and rounded to the nearest e4m3fn code, ties
+ * to even, magnitudes above 448 (and infinities) saturated to 448, NaN kept
+ * as NaN; sk_paged_decode_attn then multiplies the codes back by the same
+ * scales.
+ * A negative slot writes nothing for that token.  A slot at or past
+ * num_blocks * page_size writes nothing and sets SK_DEV_BAD_BLOCK in the
+ * device status word.  Two tokens with the same slot leave that row
+ * undefined (either token's values).
+ *
+ * Layouts (device, caller-owned): key, value bf16 [num_tokens, num_kv_heads,
+ * head_dim]; slot_mapping int64 [num_tokens]; kv_pages [num_blocks,
+ * num_kv_heads, page_size, 2*head_dim] of bf16 or e4m3fn, written in place.
+ * key, value and kv_pages must be 16-byte aligned; head_dim must be 128 and
+ * page_size 16.  Asynchronous on `stream`, no allocation, capture safe.
+ * Returns SK_OK or a negative sk_status. */
+int sk_reshape_and_cache(const void *key, const void *value, const int64_t *slot_mapping,
+                         int num_tokens, int num_kv_heads, int head_dim, void *kv_pages, int kv_dtype,
+                         float k_scale, float v_scale, int num_blocks, int page_size, void *stream);
+
 /* The whole attention call -- plan (use_plan != 0) or fixed split, split-KV
  * attention, merge -- without any device allocation, for callers that cannot
  * allocate: a host engine that owns all device memory through its own

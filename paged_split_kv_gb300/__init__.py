@@ -67,6 +67,8 @@ def lib():
                                            P, P, P, P]
         L.sk_merge_segments.restype = i32
         L.sk_merge_segments.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, P, P, P]
+        L.sk_reshape_and_cache.restype = i32
+        L.sk_reshape_and_cache.argtypes = [P, P, P, i32, i32, i32, P, i32, f32, f32, i32, i32, P]
         L.sk_get_device_status.restype = i32
         L.sk_get_device_status.argtypes = [P, i32]
         L.sk_paged_decode_attention_static.restype = i32
@@ -206,6 +208,28 @@ def sk_merge_segments(part_o, part_m, part_l, tok_nseg, out, lse=None, fixed_nse
                                  int(fixed_nseg), nt, hq, d, seg_max, _ptr(out), _ptr(lse),
                                  _stream(stream))
     return _check(rc, "sk_merge_segments")
+
+
+def sk_reshape_and_cache(key, value, slot_mapping, kv_pages, *, k_scale: float = 1.0,
+                         v_scale: float = 1.0, stream=None) -> int:
+    """Writes this step's K/V rows ([num_tokens, num_kv_heads, head_dim] bf16) into
+    ``kv_pages`` ([num_blocks, num_kv_heads, page, 2*head_dim], bf16 or e4m3) at
+    ``slot_mapping`` (int64 [num_tokens], negative = no slot), in place."""
+    import torch
+    _need(key, torch.bfloat16, "key", 3)
+    _need(value, torch.bfloat16, "value", 3)
+    _need(slot_mapping, torch.int64, "slot_mapping", 1)
+    _need(kv_pages, None, "kv_pages", 4)
+    nt, hkv, d = key.shape
+    if tuple(value.shape) != (nt, hkv, d) or slot_mapping.numel() != nt:
+        raise ValueError("key, value and slot_mapping must agree on [num_tokens, num_kv_heads, head_dim]")
+    nb, hkv2, page, d2 = kv_pages.shape
+    if hkv2 != hkv or d2 != 2 * d:
+        raise ValueError("kv_pages must be [num_blocks, num_kv_heads, page, 2 * head_dim]")
+    rc = lib().sk_reshape_and_cache(_ptr(key), _ptr(value), _ptr(slot_mapping), nt, hkv, d,
+                                    _ptr(kv_pages), _kv_dtype(kv_pages), float(k_scale), float(v_scale),
+                                    nb, page, _stream(stream))
+    return _check(rc, "sk_reshape_and_cache")
 
 
 def sk_static_scratch_bytes() -> int:

@@ -1,6 +1,7 @@
 // C ABI of libsk: argument validation, the plan cache, the device status
 // word and kernel dispatch.  See include/sk.h for the contract of each call.
 #include <cuda_runtime.h>
+#include <math.h>
 #include <stdarg.h>
 #include <stdint.h>
 #include <stdio.h>
@@ -40,6 +41,27 @@ int *g_status_ptr[kMaxDevices];
 std::mutex g_status_mutex;
 
 // Address of this device's status word (looked up once per device).
+// SM count of the current device, read once per device.
+int sm_count(int *out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail(SK_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    static std::atomic<int> cached[kMaxDevices];
+    int v = cached[dev].load();
+    if (v == 0) {
+        e = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
+        cached[dev].store(v);
+    }
+    *out = v;
+    return SK_OK;
+}
+
 int status_ptr(int **out)
 {
     int dev = 0;
@@ -309,6 +331,44 @@ int sk_merge_segments(const float *part_o, const float *part_m, const float *par
                                  static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return cuda_fail(e, "merge kernel launch");
+    return SK_OK;
+}
+
+int sk_reshape_and_cache(const void *key, const void *value, const int64_t *slot_mapping,
+                         int num_tokens, int num_kv_heads, int head_dim, void *kv_pages, int kv_dtype,
+                         float k_scale, float v_scale, int num_blocks, int page_size, void *stream)
+{
+    if (num_tokens < 0 || num_kv_heads < 1 || num_blocks < 1)
+        return fail(SK_ERR_INVALID, "sk_reshape_and_cache: num_tokens=%d num_kv_heads=%d num_blocks=%d",
+                    num_tokens, num_kv_heads, num_blocks);
+    if (kv_dtype != SK_KV_BF16 && kv_dtype != SK_KV_FP8_E4M3)
+        return fail(SK_ERR_INVALID, "sk_reshape_and_cache: kv_dtype=%d", kv_dtype);
+    if (head_dim != kHeadDim)
+        return fail(SK_ERR_UNSUPPORTED, "sk_reshape_and_cache: head_dim=%d (only 128)", head_dim);
+    if (page_size != kPage)
+        return fail(SK_ERR_UNSUPPORTED, "sk_reshape_and_cache: page_size=%d (only 16)", page_size);
+    if (kv_dtype == SK_KV_FP8_E4M3 && !(k_scale > 0.f && v_scale > 0.f && k_scale < INFINITY && v_scale < INFINITY))
+        return fail(SK_ERR_INVALID, "sk_reshape_and_cache: scales must be positive and finite");
+    if (num_tokens == 0)
+        return SK_OK;
+    if (key == nullptr || value == nullptr || slot_mapping == nullptr || kv_pages == nullptr)
+        return fail(SK_ERR_INVALID, "sk_reshape_and_cache: null pointer argument");
+    if ((reinterpret_cast<uintptr_t>(key) | reinterpret_cast<uintptr_t>(value) |
+         reinterpret_cast<uintptr_t>(kv_pages)) & 15)
+        return fail(SK_ERR_INVALID, "sk_reshape_and_cache: key, value and kv_pages must be 16-byte aligned");
+    int *status = nullptr;
+    int rc = status_ptr(&status);
+    if (rc != SK_OK)
+        return rc;
+    int sms = 0;
+    rc = sm_count(&sms);
+    if (rc != SK_OK)
+        return rc;
+    cudaError_t e = launch_kv_write(static_cast<const uint16_t *>(key), static_cast<const uint16_t *>(value),
+                                    slot_mapping, num_tokens, num_kv_heads, num_blocks, kv_pages, kv_dtype,
+                                    k_scale, v_scale, status, sms, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "kv write kernel launch");
     return SK_OK;
 }
 

@@ -110,6 +110,10 @@ cudaError_t launch_attn_simt(const AttnParams &p, int kv_dtype, cudaStream_t str
 // use for a call, or 0 when the call goes to the CUDA-core kernel.
 int attn_tc_rows(int kv_dtype, int rows_max, long long num_blocks, int H_kv);
 cudaError_t launch_attn_tc(const AttnParams &p, int kv_dtype, int rp, cudaStream_t stream);
+cudaError_t launch_kv_write(const uint16_t *key, const uint16_t *value, const int64_t *slot_mapping,
+                            int num_tokens, int num_kv_heads, long long num_blocks, void *pages,
+                            int kv_dtype, float k_scale, float v_scale, int *status, int num_sms,
+                            cudaStream_t stream);
 cudaError_t launch_merge(const float *part_o, const float *part_m, const float *part_l,
                          const int32_t *tok_nseg, int fixed_nseg, int num_tokens, int H_q,
                          int seg_max, uint16_t *out, float *lse, cudaStream_t stream);

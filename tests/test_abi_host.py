@@ -90,6 +90,25 @@ def test_merge_rejects_bad_arguments_without_cuda(sklib):
     assert f(None, FAKE, FAKE, None, 1, 4, 8, 128, 64, FAKE, None, None) == -1
 
 
+def test_kv_write_rejects_bad_arguments_without_cuda(sklib):
+    f = sklib.sk_reshape_and_cache
+
+    def call(k=FAKE, v=FAKE, sm=FAKE, nt=4, h=2, d=128, pg=FAKE, dt=0, ks=1.0, vs=1.0, nb=8, page=16):
+        return f(k, v, sm, nt, h, d, pg, dt, ks, vs, nb, page, None)
+    assert call(d=64) == -3
+    assert call(page=32) == -3
+    assert call(dt=2) == -1
+    assert call(nt=-1) == -1
+    assert call(h=0) == -1
+    assert call(nb=0) == -1
+    assert call(dt=1, ks=0.0) == -1
+    assert call(dt=1, vs=float("inf")) == -1
+    assert call(k=None) == -1
+    assert call(sm=None) == -1
+    assert call(pg=ctypes.c_void_p(264)) == -1          # not 16-byte aligned
+    assert call(nt=0, k=None, v=None, sm=None, pg=None) == 0   # nothing to write: no launch
+
+
 def test_python_binding_refuses_cpu_tensors(sklib):
     import torch
     import paged_split_kv_gb300 as sk

@@ -31,7 +31,7 @@ def _rank(rank, world, port, elapsed, out):
 def test_max_over_two_gloo_ranks():
     world, port = 2, _free_port()
     elapsed = [12.5, 40.25]
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()
     mp.spawn(_rank, args=(world, port, elapsed, out), nprocs=world, join=True)
     assert out[0] == out[1] == 40.25
 
