@@ -54,6 +54,8 @@ def _args():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--forward-layers", type=int, default=0,
+                    help="time a CUDA-graph forward: one plan + this many layers of attention + merge")
     ap.add_argument("--kv-write", choices=["bf16", "fp8"], default=None,
                     help="time the KV write step (65536 tokens x 8 KV heads) instead of the path")
     ap.add_argument("--fixed-split", action="store_true",
@@ -533,8 +535,96 @@ def run_kv_write(a, local):
     return 0
 
 
+def run_forward(a, w, local):
+    """One forward as a CUDA graph: the plan once, then `layers` x (attention +
+    merge), replayed.  A second graph without the plan gives the plan's share.
+    Every layer reads the same K/V cache; it is larger than L2, so each layer
+    streams it from HBM as a layer of its own would."""
+    import torch
+    import paged_split_kv_gb300 as sk
+    if not os.path.exists(sk.LIB_PATH):
+        from paged_split_kv_gb300 import build as b
+        b.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    L = a.forward_layers
+    if w.kv_bytes <= 129e6:
+        raise SystemExit("--forward-layers needs a workload larger than L2")
+    q = si.make_q(w, dev)
+    kv = si.make_kv(w, dev)
+    bt = torch.as_tensor(w.block_table, device=dev)
+    lens = torch.as_tensor(w.seq_lens, device=dev)
+    cu = torch.as_tensor(w.cu_q, device=dev)
+    nt, hkv, nsm = w.num_tokens, w.num_kv_heads, w.num_sms
+    use_plan = w.bs > 1
+    plan = torch.empty(sk.plan_capacity(w.bs, hkv, nsm), dtype=torch.int32, device=dev) if use_plan else None
+    tok = torch.empty(nt, dtype=torch.int32, device=dev) if use_plan else None
+    part_o = torch.empty((nt, w.seg_max, w.num_q_heads, w.head_dim), dtype=torch.float32, device=dev)
+    part_m = torch.empty((nt, w.seg_max, w.num_q_heads), dtype=torch.float32, device=dev)
+    part_l = torch.empty_like(part_m)
+    outs = [torch.empty((nt, w.num_q_heads, w.head_dim), dtype=torch.bfloat16, device=dev) for _ in range(L)]
+    fixed = 0 if use_plan else sk.sk_fixed_nseg(w.bs, hkv, nsm, w.seg_max)
+    side = torch.cuda.Stream()
+
+    def layers(stream, with_plan):
+        if with_plan and use_plan:
+            sk.sk_build_plan(lens, cu, hkv, plan, tok, nsm, w.seg_max, stream)
+        for i in range(L):
+            sk.sk_paged_decode_attn(q, kv, bt, lens, cu, plan, part_o, part_m, part_l, max_q_len=w.max_q_len,
+                                    sm_scale=w.sm_scale, num_sms=nsm, k_scale=w.k_scale, v_scale=w.v_scale,
+                                    causal=bool(w.causal), stream=stream)
+            sk.sk_merge_segments(part_o, part_m, part_l, tok, outs[i], None, fixed_nseg=fixed, stream=stream)
+
+    graphs = {}
+    with torch.cuda.stream(side):
+        for with_plan in (True, False):
+            sk.sk_plan_cache_reset()
+            layers(side, with_plan)          # warm (and plan) outside capture
+            side.synchronize()
+            sk.sk_plan_cache_reset()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                layers(side, with_plan)
+            graphs[with_plan] = g
+    torch.cuda.synchronize()
+    res = {}
+    sampler = ClockSampler(local)
+    sampler.start()
+    for with_plan in (True, False):
+        g = graphs[with_plan]
+        for _ in range(max(3, a.warmup)):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(a.steps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        res[with_plan] = e0.elapsed_time(e1) / a.steps
+    clocks = sampler.stop()
+    if sk.sk_get_device_status(clear=True):
+        raise RuntimeError("device status set during the forward")
+    ms = res[True]
+    tbps = L * w.kv_bytes / (ms * 1e-3) / 1e12
+    line = {"metric": METRIC + f" (graph-captured forward, {L} layers)", "value": round(tbps, 4), "unit": "TB/s",
+            "n_gpus": 1, "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(ms, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if w.kv_dtype == si.KV_BF16 else "fp8_e4m3",
+            "data": "synthetic; one K/V cache read by every layer (larger than L2)",
+            "config": _config_json(w, {"layers": L, "split": "plan" if use_plan else "fixed",
+                                       "graph": "one plan + layers x (attention + merge) per replay"}),
+            "us_per_layer": round(1e3 * res[False] / L, 2),
+            "us_plan_per_forward": round(1e3 * (res[True] - res[False]), 2),
+            "clocks": clocks, "gpu_launches": a.steps * (2 * L + (1 if use_plan else 0))}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     a = _args()
+    if a.forward_layers > 0:
+        return run_forward(a, si.config(a.config), int(os.environ.get("LOCAL_RANK", 0)))
     if a.kv_write:
         return run_kv_write(a, int(os.environ.get("LOCAL_RANK", 0)))
     ws, rank, local = _dist()
