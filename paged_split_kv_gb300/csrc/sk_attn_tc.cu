@@ -60,7 +60,6 @@ using namespace sm100;
 constexpr int kTokTile = 128;                       // tokens per tile (MMA M)
 constexpr int kPagesPerTile = kTokTile / kPage;     // 8
 constexpr int kChunkRegion = kTokTile * 128;        // 16 KB: 128 token rows of 128 B
-constexpr int kStageBytes = 4 * kChunkRegion;       // 64 KB
 constexpr int kSoftmaxWarp0 = 2;
 constexpr int kSoftmaxGroups = 2;                   // warpgroups splitting the query rows
 constexpr int kSoftmaxWarps = 4 * kSoftmaxGroups;
@@ -89,8 +88,16 @@ struct Cfg {
     // P alone (with 64 rows the softmax needs the registers; it converts V itself)
     static constexpr bool kConvWarps = FP8 && RP <= 32;
     static constexpr int kThreads = 32 * (kConvWarp0 + (kConvWarps ? 4 : 0));   // 352 or 480
-    static constexpr int kStages = (3 * kStageBytes + kQBytes + kMiscBytes <= kMaxSmem) ? 3 : 2;
-    static constexpr int kOffQ = kStages * kStageBytes;
+    // With converter warps the f16 V lives in a ring of its own (freed by the PV that read
+    // it), so a stage holds only the 32 KB of codes and four stages fit; otherwise a stage
+    // is 64 KB (bf16 rows, or fp8 codes plus their f16 V).
+    static constexpr bool kVRing = kConvWarps;
+    static constexpr int kStageBytes = kVRing ? 2 * kChunkRegion : 4 * kChunkRegion;
+    static constexpr int kVBufBytes = 2 * kChunkRegion;      // f16 V of one tile
+    static constexpr int kVBufs = kVRing ? 2 : 0;
+    static constexpr int kStages = kVRing ? 4 : (3 * kStageBytes + kQBytes + kMiscBytes <= kMaxSmem) ? 3 : 2;
+    static constexpr int kOffVRing = kStages * kStageBytes;
+    static constexpr int kOffQ = kOffVRing + kVBufs * kVBufBytes;
     static constexpr int kOffMisc = kOffQ + kQBytes;
     static constexpr int kSmemBytes = kOffMisc + kMiscBytes;
     static constexpr int kTmemCols = (3 * RP <= 64) ? 64 : (3 * RP <= 128) ? 128 : 256;
@@ -99,7 +106,7 @@ struct Cfg {
     static constexpr int kPageBytes = 2 * kGroupBytes;        // one page (one TMA copy)
     // V operand: bf16 chunks 2-3 of the raw rows (atoms 1 KB apart along the dimensions,
     // groups kGroupBytes apart), or the converted f16 (atoms 16 KB apart, groups 1 KB apart)
-    static constexpr int kOffV = FP8 ? 2 * kChunkRegion : 2048;
+    static constexpr int kOffV = FP8 ? 2 * kChunkRegion : 2048;   // within a stage (not used with kVRing)
     static constexpr int kVDimStride = FP8 ? kChunkRegion : 1024;
     static constexpr int kVGroupStride = FP8 ? 1024 : kGroupBytes;
     // misc area
@@ -109,12 +116,13 @@ struct Cfg {
     static constexpr int kBarSFree = kBarSFull + 16;         // [2]
     static constexpr int kBarPFull = kBarSFree + 16;         // [2], by tile parity
     static constexpr int kBarODone = kBarPFull + 16;         // committed once, after the last PV
-    static constexpr int kBarVReady = kBarODone + 8;         // [kStages]: V converted (converter warps)
-    static constexpr int kTmemSlot = kBarVReady + 8 * kStages;
+    static constexpr int kBarVReady = kBarODone + 8;         // [2]: V ring buffer filled (converter warps)
+    static constexpr int kBarVFree = kBarVReady + 16;        // [2]: V ring buffer read (its PV completed)
+    static constexpr int kTmemSlot = kBarVFree + 16;
     static constexpr int kAbort = kTmemSlot + 4;
     static constexpr int kPvIssued = kAbort + 4;             // int: PVs issued so far (written by the PV thread)
     static constexpr int kFlags = kPvIssued + 4;             // int[group][3][4]: per tile parity, then the epilogue
-    static constexpr int kRed = 256;                         // float[group][4][32]
+    static constexpr int kRed = 320;                         // float[group][4][32]
     static constexpr int kMrun = kRed + kSoftmaxGroups * 4 * 32 * 4;   // float[64] running max (log2 units)
     static constexpr int kMthr = kMrun + 64 * 4;             // float[64] running max + rescale threshold
     static constexpr int kMsub = kMthr + 64 * 4;             // float[64] running max with -inf -> 0
@@ -123,6 +131,7 @@ struct Cfg {
     static_assert(kFlags + kSoftmaxGroups * 48 <= kRed, "misc area");
     static_assert(kCrow + 64 * 4 <= kMiscBytes, "misc area");
     static_assert(kSmemBytes <= kMaxSmem, "shared memory");
+    static_assert(kStages <= 8, "barrier area");
     static_assert((kOffQ % 1024) == 0 && (kMrun % 16) == 0 && (kMthr % 16) == 0 && (kMsub % 16) == 0 &&
                       (kCrow % 16) == 0,
                   "operand and vector alignment");
@@ -225,12 +234,13 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 
 // fp8: 16-byte unit u (dims 16u..16u+15) of token tau's V code row in stage `sb`
 // (TMA-swizzled) to f16, written as units 2(u%4), 2(u%4)+1 of the token's row in
-// the MN-major operand atom of dims [64(u/4), 64(u/4)+64); zeros if `zero`.
-template <int kGroupBytes, int kOffV>
-__device__ __forceinline__ void convert_v_unit(uint8_t *sb, int tau, int u, bool zero)
+// the MN-major operand atom of dims [64(u/4), 64(u/4)+64) of the f16 V at `vdst`;
+// zeros if `zero`.
+template <int kGroupBytes>
+__device__ __forceinline__ void convert_v_unit(const uint8_t *sb, uint8_t *vdst, int tau, int u, bool zero)
 {
     const uint8_t *vraw = sb + (tau >> 3) * kGroupBytes + 1024 + (tau & 7) * 128;
-    uint8_t *atom = sb + kOffV + (u >> 2) * kChunkRegion + (tau >> 3) * 1024 + (tau & 7) * 128;
+    uint8_t *atom = vdst + (u >> 2) * kChunkRegion + (tau >> 3) * 1024 + (tau & 7) * 128;
     uint4 cv = *reinterpret_cast<const uint4 *>(vraw + ((u ^ (tau & 7)) << 4));
     if (zero)
         cv = make_uint4(0u, 0u, 0u, 0u);
@@ -286,7 +296,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
     const uint32_t bar_odone = mbase + C::kBarODone;
     auto bar_vready = [&](int s) { return mbase + C::kBarVReady + 8 * s; };
     const uint32_t q_s = sbase + C::kOffQ;
-    auto stage = [&](int s) { return sbase + (uint32_t)(s * kStageBytes); };
+    auto stage = [&](int s) { return sbase + (uint32_t)(s * C::kStageBytes); };
+    auto bar_vfree = [&](int v) { return mbase + C::kBarVFree + 8 * v; };
 
     const int k0 = w.k0, k1 = w.k1;
     const int ntiles = k1 > k0 ? (k1 - k0 + kTokTile - 1) / kTokTile : 0;
@@ -296,7 +307,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(bar_full(s), 1);
             mbar_init(bar_empty(s), 1);
-            mbar_init(bar_vready(s), 4);
+        }
+        for (int v = 0; v < 2; ++v) {
+            mbar_init(bar_vready(v), 4);
+            mbar_init(bar_vfree(v), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_sfull(b), 1);
@@ -447,7 +461,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
         constexpr uint32_t idesc_qk = FP8 ? idesc_e4m3_f32(kTokTile, RP, 0, 0) : idesc_bf16_f32(kTokTile, RP, 0, 0);
         constexpr uint32_t idesc_pv = FP8 ? idesc_f16_f32(kTokTile, RP, 1, 1) : idesc_bf16_f32(kTokTile, RP, 1, 1);
         const uint64_t d_kv0 = smem_desc_sw128(stage(0), 16, C::kGroupBytes);           // K-major K tile
-        const uint64_t d_v0 = smem_desc_sw128(stage(0) + C::kOffV, C::kVDimStride, C::kVGroupStride);  // MN-major V^T
+        const uint64_t d_v0 = C::kVRing ? smem_desc_sw128(sbase + C::kOffVRing, C::kVDimStride, C::kVGroupStride)
+                                        : smem_desc_sw128(stage(0) + C::kOffV, C::kVDimStride, C::kVGroupStride);  // MN-major V^T
         const uint64_t d_p0 = smem_desc_sw128(stage(0), 1024, C::kGroupBytes);          // MN-major P^T
         const uint64_t d_q0 = smem_desc_sw128(q_s, 16, 1024);                          // K-major Q
         auto adv = [](uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); };
@@ -475,7 +490,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                 if (!ok)
                     break;
                 tc_fence_after();
-                const uint32_t so = (uint32_t)(st * kStageBytes);
+                const uint32_t so = (uint32_t)(st * C::kStageBytes);
                 if constexpr (FP8) {
 #pragma unroll
                     for (int t = 0; t < 2; ++t)
@@ -507,18 +522,21 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             // stage (empty), which is also how the softmax learns that O holds tile i.
             for (int i = 0; i < ntiles && ok; ++i) {
                 ok = mbar_wait_bounded(bar_pfull(i & 1), (i >> 1) & 1, abort_flag, kWaitLimit);
-                if (C::kConvWarps && ok)   // V(i) in f16; its phase cannot run ahead: tile i+kStages needs PV(i)
-                    ok = mbar_wait_bounded(bar_vready(i % C::kStages), (i / C::kStages) & 1, abort_flag, kWaitLimit);
+                if (C::kVRing && ok)   // V(i) in f16; its phase cannot run ahead: V(i+2) needs PV(i) done
+                    ok = mbar_wait_bounded(bar_vready(i & 1), (i >> 1) & 1, abort_flag, kWaitLimit);
                 ok = __all_sync(kFull, ok);
                 if (!ok)
                     break;
                 tc_fence_after();
-                const uint32_t so = (uint32_t)((i % C::kStages) * kStageBytes);    // P^T over the dead K area
+                const uint32_t so = (uint32_t)((i % C::kStages) * C::kStageBytes);    // P^T over the dead K area
+                const uint32_t vo = C::kVRing ? (uint32_t)((i & 1) * C::kVBufBytes) : so;
 #pragma unroll
                 for (int k = 0; k < kPagesPerTile; ++k)
-                    mma_f16_ss_warp(tmem_o, adv(d_v0, so + k * 2 * C::kVGroupStride), adv(d_p0, so + k * 2 * C::kGroupBytes),
+                    mma_f16_ss_warp(tmem_o, adv(d_v0, vo + k * 2 * C::kVGroupStride), adv(d_p0, so + k * 2 * C::kGroupBytes),
                                     idesc_pv, (i > 0 || k > 0) ? 1u : 0u);
                 mma_commit_warp(bar_empty(i % C::kStages));
+                if constexpr (C::kVRing)
+                    mma_commit_warp(bar_vfree(i & 1));
                 last = i;
                 __syncwarp();
                 if (lane == 0)
@@ -539,28 +557,30 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
     } else if (C::kConvWarps && warp >= kConvWarp0) {
         // ================================================================ fp8 V converters
         // One thread per token row of the tile: its 128 V codes to f16 in the MN-major operand
-        // layout as soon as the tile lands (rows past L in the last page become zeros), then
-        // the stage's vready barrier tells the PV issuer.  The converted area of a stage is
-        // rewritten only after its next load, which waits for the PV that read it.
+        // layout of V ring buffer j % 2 as soon as the tile lands and PV(j-2) has read that
+        // buffer (rows past L in the last page become zeros); vready tells the PV issuer.
         const int tau = (warp - kConvWarp0) * 32 + lane;
         const int last_page_end = (w.L + kPage - 1) / kPage * kPage;
         bool ok = true;
         for (int j = 0; j < ntiles; ++j) {
-            const int st = j % C::kStages;
+            const int st = j % C::kStages, vb = j & 1;
             ok = mbar_wait_bounded(bar_full(st), (j / C::kStages) & 1, abort_flag, kWaitLimit);
+            if (ok && j >= 2)      // the buffer's previous tile, j-2, has been read by its PV
+                ok = mbar_wait_bounded(bar_vfree(vb), ((j >> 1) - 1) & 1, abort_flag, kWaitLimit);
             ok = __all_sync(kFull, ok);
             if (!ok)
                 break;
             const int tokv = k0 + j * kTokTile + tau;
             const bool zero = tokv >= w.L && tokv < last_page_end;
-            uint8_t *sb = smem + st * kStageBytes;
+            const uint8_t *sb = smem + st * C::kStageBytes;
+            uint8_t *vdst = smem + C::kOffVRing + vb * C::kVBufBytes;
 #pragma unroll
             for (int u = 0; u < 8; ++u)
-                convert_v_unit<C::kGroupBytes, C::kOffV>(sb, tau, u, zero);
+                convert_v_unit<C::kGroupBytes>(sb, vdst, tau, u, zero);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(bar_vready(st));
+                mbar_arrive(bar_vready(vb));
         }
         if (!ok && lane == 0) {
             *abort_flag = 1;
@@ -596,7 +616,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             const bool zero = !got || (tokv >= w.L && tokv < last_page_end);
 #pragma unroll
             for (int uu = 0; uu < 4; ++uu)
-                convert_v_unit<C::kGroupBytes, C::kOffV>(smem + stv * kStageBytes, tau, 4 * wg + uu, zero);
+                convert_v_unit<C::kGroupBytes>(smem + stv * C::kStageBytes, smem + stv * C::kStageBytes + C::kOffV, tau,
+                                               4 * wg + uu, zero);
             return got;
         };
         if constexpr (FP8 && !C::kConvWarps) {
@@ -720,7 +741,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                 // probabilities against the running max (masked entries are -inf -> 0), written as
                 // this token's row of P^T over the tile's K area, which QK(j) no longer needs:
                 // MN-major, 128-byte swizzle, 16-byte unit u of row tau stored at u ^ (tau % 8)
-                uint8_t *prow = smem + st * kStageBytes + (tau >> 3) * C::kGroupBytes + (tau & 7) * 128;
+                uint8_t *prow = smem + st * C::kStageBytes + (tau >> 3) * C::kGroupBytes + (tau & 7) * 128;
 #pragma unroll
                 for (int u = 0; u < RH / 8; ++u) {
                     const float4 ma = *reinterpret_cast<const float4 *>(m_sub + r0 + 8 * u);
@@ -742,7 +763,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                 const bool tail_row = tok >= w.L && tok < last_page_end;   // past L in the last page: anything
                 if (!FP8 && tail_row) {
                     // V dims [64 wg, 64 wg + 64) of this row: chunk 2 + wg
-                    uint8_t *vrow = smem + st * kStageBytes + C::kOffV + wg * 1024 + (tau >> 3) * C::kGroupBytes +
+                    uint8_t *vrow = smem + st * C::kStageBytes + C::kOffV + wg * 1024 + (tau >> 3) * C::kGroupBytes +
                                     (tau & 7) * 128;
 #pragma unroll
                     for (int u = 0; u < 8; ++u)
