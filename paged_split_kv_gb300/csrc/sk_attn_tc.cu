@@ -65,6 +65,7 @@ constexpr int kSoftmaxGroups = 2;                   // warpgroups splitting the 
 constexpr int kSoftmaxWarps = 4 * kSoftmaxGroups;
 constexpr int kPvWarp = kSoftmaxWarp0 + kSoftmaxWarps;   // 10: issues the PV products
 constexpr int kConvWarp0 = kPvWarp + 1;             // 11-14: fp8 V converters, where present
+constexpr int kSBufs = 4;                           // S^T buffers in TMEM (QK may run this far ahead of PV)
 constexpr float kRescaleLog2 = 8.0f;
 constexpr long long kWaitLimit = 4000000000LL;      // cycles (~2 s)
 constexpr uint32_t kFull = 0xffffffffu;
@@ -100,7 +101,7 @@ struct Cfg {
     static constexpr int kOffQ = kOffVRing + kVBufs * kVBufBytes;
     static constexpr int kOffMisc = kOffQ + kQBytes;
     static constexpr int kSmemBytes = kOffMisc + kMiscBytes;
-    static constexpr int kTmemCols = (3 * RP <= 64) ? 64 : (3 * RP <= 128) ? 128 : 256;
+    static constexpr int kTmemCols = ((kSBufs + 1) * RP <= 128) ? 128 : ((kSBufs + 1) * RP <= 256) ? 256 : 512;
     static constexpr uint32_t kTxBytes = FP8 ? 2 * kChunkRegion : 4 * kChunkRegion;   // bytes the TMA brings per stage
     static constexpr int kGroupBytes = FP8 ? 2048 : 4096;     // one 8-token group of the raw rows
     static constexpr int kPageBytes = 2 * kGroupBytes;        // one page (one TMA copy)
@@ -112,10 +113,10 @@ struct Cfg {
     // misc area
     static constexpr int kBarFull = 0;                       // [kStages]
     static constexpr int kBarEmpty = 8 * kStages;            // [kStages]
-    static constexpr int kBarSFull = 16 * kStages;           // [2]
-    static constexpr int kBarSFree = kBarSFull + 16;         // [2]
-    static constexpr int kBarPFull = kBarSFree + 16;         // [2], by tile parity
-    static constexpr int kBarODone = kBarPFull + 16;         // committed once, after the last PV
+    static constexpr int kBarSFull = 16 * kStages;           // [kSBufs]
+    static constexpr int kBarSFree = kBarSFull + 8 * kSBufs; // [kSBufs]
+    static constexpr int kBarPFull = kBarSFree + 8 * kSBufs; // [kSBufs], by S buffer
+    static constexpr int kBarODone = kBarPFull + 8 * kSBufs; // committed once, after the last PV
     static constexpr int kBarVReady = kBarODone + 8;         // [2]: V ring buffer filled (converter warps)
     static constexpr int kBarVFree = kBarVReady + 16;        // [2]: V ring buffer read (its PV completed)
     static constexpr int kTmemSlot = kBarVFree + 16;
@@ -312,7 +313,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             mbar_init(bar_vready(v), 4);
             mbar_init(bar_vfree(v), 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kSBufs; ++b) {
             mbar_init(bar_sfull(b), 1);
             mbar_init(bar_sfree(b), kSoftmaxWarps);
             mbar_init(bar_pfull(b), kSoftmaxWarps);
@@ -401,7 +402,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
     tc_fence_after();
     }
     const uint32_t tmem = warp != 0 ? *reinterpret_cast<volatile uint32_t *>(misc + C::kTmemSlot) : 0u;
-    const uint32_t tmem_s0 = tmem, tmem_o = tmem + 2 * RP;
+    const uint32_t tmem_s0 = tmem, tmem_o = tmem + kSBufs * RP;
 
     if (warp == 0) {
         // ================================================================ TMA producer
@@ -469,17 +470,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
         bool ok = true;
         int last = -1;
         if (warp == 1) {
-            // QK(j) once tile j has landed, its S buffer is free, and PV(j-2) is issued.  The last
-            // condition keeps barrier phases unambiguous: P_full[b] cannot run two tiles ahead of
-            // its PV, and the softmax never runs more than one tile ahead of the PVs it waits on.
+            // QK(j) once tile j has landed, its S buffer (j % kSBufs) is free, and PV(j - kSBufs)
+            // is issued.  The last condition keeps barrier phases unambiguous: P_full[b] cannot
+            // run a full round of buffers ahead of its PV.
             for (int j = 0; j < ntiles && ok; ++j) {
-                const int st = j % C::kStages, b = j & 1;
+                const int st = j % C::kStages, b = j % kSBufs;
                 ok = mbar_wait_bounded(bar_full(st), (j / C::kStages) & 1, abort_flag, kWaitLimit);
-                if (ok && j >= 2)
-                    ok = mbar_wait_bounded(bar_sfree(b), ((j - 2) >> 1) & 1, abort_flag, kWaitLimit);
-                if (ok && *pv_issued < j - 1) {
+                if (ok && j >= kSBufs)
+                    ok = mbar_wait_bounded(bar_sfree(b), ((j / kSBufs) - 1) & 1, abort_flag, kWaitLimit);
+                if (ok && *pv_issued < j - kSBufs + 1) {
                     const long long t0 = clock64();
-                    while (*pv_issued < j - 1) {
+                    while (*pv_issued < j - kSBufs + 1) {
                         if (*abort_flag || clock64() - t0 > kWaitLimit) {
                             ok = false;
                             break;
@@ -515,13 +516,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                     atomicOr(p.status, SK_DEV_TIMEOUT);
                 }
                 if (last >= 0)     // let this warp's MMAs finish before TMEM is freed
-                    mbar_wait_bounded(bar_sfull(last & 1), (last >> 1) & 1, nullptr, kWaitLimit);
+                    mbar_wait_bounded(bar_sfull(last % kSBufs), (last / kSBufs) & 1, nullptr, kWaitLimit);
             }
         } else {
             // PV(i) as soon as the softmax threads have written P(i).  Its completion frees the
             // stage (empty), which is also how the softmax learns that O holds tile i.
             for (int i = 0; i < ntiles && ok; ++i) {
-                ok = mbar_wait_bounded(bar_pfull(i & 1), (i >> 1) & 1, abort_flag, kWaitLimit);
+                ok = mbar_wait_bounded(bar_pfull(i % kSBufs), (i / kSBufs) & 1, abort_flag, kWaitLimit);
                 if (C::kVRing && ok)   // V(i) in f16; its phase cannot run ahead: V(i+2) needs PV(i) done
                     ok = mbar_wait_bounded(bar_vready(i & 1), (i >> 1) & 1, abort_flag, kWaitLimit);
                 ok = __all_sync(kFull, ok);
@@ -630,22 +631,23 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             lsum[r] = 0.f;
 
         for (int j = 0; j < ntiles; ++j) {
-            const int b = j & 1;
+            const int b = j & 1;                // flags slot
+            const int sb = j % kSBufs;          // S buffer and its barriers
             const int st = j % C::kStages;
             float x[RH];
-            bool ok = !failed && mbar_wait_bounded(bar_sfull(b), (j >> 1) & 1, abort_flag, kWaitLimit);
+            bool ok = !failed && mbar_wait_bounded(bar_sfull(sb), (j / kSBufs) & 1, abort_flag, kWaitLimit);
             ok = __all_sync(kFull, ok);          // tcgen05.ld is warp-collective
             if (ok) {
                 tc_fence_after();
 #pragma unroll
                 for (int c = 0; c < RH; c += kLd)
-                    tmem_ld32<kLd>(tmem_s0 + b * RP + r0 + c + lane_off, x + c);
+                    tmem_ld32<kLd>(tmem_s0 + sb * RP + r0 + c + lane_off, x + c);
                 tmem_wait_ld();
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(bar_sfree(b));
+                mbar_arrive(bar_sfree(sb));
             // mask and scale: this thread's key is `tok`; row r = j' * G + i sees it when
             // tok < segment end and (causal) j' >= tok - (L - q_len)
             const int tok = k0 + j * kTokTile + tau;
@@ -774,7 +776,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(bar_pfull(b));
+                mbar_arrive(bar_pfull(sb));
             // fp8: the next tile's V conversion fills the wait for its S (its stage is free once it
             // has landed); the fence before that tile's P_full publishes it to the tensor core
             if (FP8 && !C::kConvWarps && !failed && j + 1 < ntiles && !convert_v(j + 1))
