@@ -12,10 +12,13 @@ they follow.
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 (values the pages print, closed forms, invariants, a library softmax on tiny
-inputs, brute force) and, for the KV write step and the e4m3fn encoder, by
+inputs, brute force); for the KV write step and the e4m3fn encoder by
 ``tests/test_kv_write_pins.py`` (round trips through the pinned decoder, IEEE
 midpoints, PyTorch's float8 cast, a hand-written page image, attention on
-directly built pages); none is marked "parity unpinned".
+directly built pages); and for the shuffled-page conversion by
+``tests/test_shuffle_pins.py`` (NumPy's reshape and transpose of the printed
+formula, a bijection on unique values, untouched blocks); none is marked
+"parity unpinned".
 """
 from __future__ import annotations
 
@@ -64,6 +67,8 @@ def _load():
         lib.sko_reshape_and_cache.restype = None
         lib.sko_reshape_and_cache.argtypes = [P, P, P, i32, i32, i32, P, i32, ctypes.c_float, ctypes.c_float,
                                               i64, i32]
+        lib.sko_std_to_shuffled.restype = None
+        lib.sko_std_to_shuffled.argtypes = [P, i32, P, i32, i64, i32, i32, i32, P, P]
         lib.sko_bf16_to_double.restype = f64
         lib.sko_bf16_to_double.argtypes = [ctypes.c_uint16]
         lib.sko_e4m3fn_to_double.restype = f64
@@ -128,6 +133,26 @@ def reshape_and_cache(key_bits, value_bits, slot_mapping, kv_pages: np.ndarray, 
     _load().sko_reshape_and_cache(_ptr(key_bits), _ptr(value_bits), _ptr(slot_mapping), nt, hkv, d,
                                   _ptr(kv_pages), int(kv_dtype), float(k_scale), float(v_scale), nb, page)
     return kv_pages
+
+
+def std_to_shuffled(kv_pages: np.ndarray, block_ids=None, k_shuf=None, v_shuf=None):
+    """Standard pages [NB, H, N, 2D] (uint16 bf16 bits or uint8 e4m3 codes) to
+    shuffled K [NB, H, D/x, N, x] and V [NB, H, N/x, D, x], x = 16 / element size.
+    Outputs are created zeroed unless given (then written in place)."""
+    kv_pages = np.ascontiguousarray(kv_pages)
+    nb, h, n, d2 = kv_pages.shape
+    d = d2 // 2
+    es = kv_pages.dtype.itemsize
+    x = 16 // es
+    if k_shuf is None:
+        k_shuf = np.zeros((nb, h, d // x, n, x), kv_pages.dtype)
+    if v_shuf is None:
+        v_shuf = np.zeros((nb, h, n // x, d, x), kv_pages.dtype)
+    assert k_shuf.flags.c_contiguous and v_shuf.flags.c_contiguous
+    ids = None if block_ids is None else _c(block_ids, np.int32)
+    _load().sko_std_to_shuffled(_ptr(kv_pages), es, _ptr(ids), 0 if ids is None else ids.shape[0], nb, h, d, n,
+                                _ptr(k_shuf), _ptr(v_shuf))
+    return k_shuf, v_shuf
 
 
 def fixed_nseg(bs: int, num_kv_heads: int, num_sms: int, seg_max: int = 64) -> int:

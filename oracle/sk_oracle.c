@@ -11,7 +11,9 @@
  *   [RFC]  vLLM RFC 59111 "NixlConnector: convert standard KV pages to ROCm
  *          AITER shuffled pages on the decode side", Background: standard
  *          pages hold, per head, token rows with K and V side by side
- *          ([H, N, 2*D]); Proposed Change: OCP e4m3fn vs e4m3fnuz.
+ *          ([H, N, 2*D]), shuffled pages K [H, D/x, N, x] and V
+ *          [H, N/x, D, x]; Proposed Change: OCP e4m3fn vs e4m3fnuz, and the
+ *          per-block conversion (Convert).
  *   [PR]   SGLang PR 39172 "[AMD] gfx950 assembly attention: length-aware
  *          split-KV for dynamic workload":
  *            Motivation    -- the fixed split max(1, min(64, pow2floor(CUs /
@@ -480,6 +482,44 @@ void sko_reshape_and_cache(const uint16_t *key, const uint16_t *value, const int
                     const float vq = (float)sko_bf16_to_double(value[src + d]) / v_scale;
                     pg[row + d] = sko_e4m3fn_encode(kq);
                     pg[row + head_dim + d] = sko_e4m3fn_encode(vq);
+                }
+            }
+        }
+    }
+}
+
+/* ---------------------------------------------------------------------------
+ * [RFC] Proposed Change, step 4 (Convert): the decode side's per-block view and
+ * permute from standard pages to AITER's shuffled pages, with x = 16 / element
+ * size (8 for bf16, 16 for e4m3).  For block blk, head h, token row n and
+ * dimension d of K = page[..., 0:D) and V = page[..., D:2D):
+ *   k_shuf[blk][h][d / x][n][d % x] = K[blk][h][n][d]     (k_shuf [NB, H, D/x, N, x])
+ *   v_shuf[blk][h][n / x][d][n % x] = V[blk][h][n][d]     (v_shuf [NB, H, N/x, D, x])
+ * for every block in block_ids (all blocks when block_ids is NULL); other
+ * blocks of the outputs are left alone, as are ids outside [0, num_blocks).
+ * Pure data movement: elements are copied as elem_size-byte units. */
+void sko_std_to_shuffled(const void *kv_pages, int elem_size, const int32_t *block_ids, int num_ids,
+                         int64_t num_blocks, int num_kv_heads, int head_dim, int page, void *k_shuf,
+                         void *v_shuf)
+{
+    const int x = 16 / elem_size;
+    const int n_ids = block_ids ? num_ids : (int)num_blocks;
+    const uint8_t *src = (const uint8_t *)kv_pages;
+    uint8_t *ko = (uint8_t *)k_shuf, *vo = (uint8_t *)v_shuf;
+    for (int i = 0; i < n_ids; ++i) {
+        const int64_t blk = block_ids ? block_ids[i] : i;
+        if (blk < 0 || blk >= num_blocks)
+            continue;
+        for (int h = 0; h < num_kv_heads; ++h) {
+            const int64_t bh = blk * num_kv_heads + h;
+            for (int n = 0; n < page; ++n) {
+                for (int d = 0; d < head_dim; ++d) {
+                    const int64_t k_src = ((bh * page + n) * 2 * head_dim + d) * elem_size;
+                    const int64_t v_src = ((bh * page + n) * 2 * head_dim + head_dim + d) * elem_size;
+                    const int64_t k_dst = (((bh * (head_dim / x) + d / x) * page + n) * x + d % x) * elem_size;
+                    const int64_t v_dst = (((bh * (page / x) + n / x) * head_dim + d) * x + n % x) * elem_size;
+                    memcpy(ko + k_dst, src + k_src, (size_t)elem_size);
+                    memcpy(vo + v_dst, src + v_src, (size_t)elem_size);
                 }
             }
         }
