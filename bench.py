@@ -56,6 +56,9 @@ def _args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--forward-layers", type=int, default=0,
                     help="time a CUDA-graph forward: one plan + this many layers of attention + merge")
+    ap.add_argument("--shuffle", choices=["bf16", "fp8"], default=None,
+                    help="time the standard -> shuffled page conversion of a whole cache "
+                         "(config 2's for bf16, config 4's for fp8)")
     ap.add_argument("--kv-write", choices=["bf16", "fp8"], default=None,
                     help="time the KV write step (65536 tokens x 8 KV heads) instead of the path")
     ap.add_argument("--fixed-split", action="store_true",
@@ -621,8 +624,59 @@ def run_forward(a, w, local):
     return 0
 
 
+def run_shuffle(a, local):
+    """The standard -> shuffled conversion of every block of a workload's cache
+    (K/V larger than L2): bytes read plus bytes written per call."""
+    import torch
+    import paged_split_kv_gb300 as sk
+    if not os.path.exists(sk.LIB_PATH):
+        from paged_split_kv_gb300 import build as b
+        b.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = si.config(2 if a.shuffle == "bf16" else 4)
+    kv = si.make_kv(w, dev, poison_tail=False)
+    nb, hkv, page, d2 = kv.shape
+    x = 16 // kv.element_size()
+    k_shuf = torch.empty((nb, hkv, d2 // 2 // x, page, x), dtype=kv.dtype, device=dev)
+    v_shuf = torch.empty((nb, hkv, page // x, d2 // 2, x), dtype=kv.dtype, device=dev)
+    f = lambda: sk.sk_std_to_shuffled(kv, k_shuf, v_shuf)
+    for _ in range(max(3, a.warmup)):
+        f()
+    torch.cuda.synchronize()
+    if sk.sk_get_device_status(clear=True):
+        raise RuntimeError("device status set by the conversion")
+    sampler = ClockSampler(local)
+    sampler.start()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.steps)]
+    for e0, e1 in evs:
+        e0.record()
+        f()
+        e1.record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
+    moved = 2 * kv.numel() * kv.element_size()
+    gbs = moved / (ms * 1e-3) / 1e9
+    peak, kind = _peaks()
+    line = {"metric": "standard -> shuffled page conversion GB/s", "value": round(gbs, 1), "unit": "GB/s",
+            "n_gpus": 1, "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(ms, 5),
+            "higher_is_better": True, "dtype": a.shuffle if a.shuffle == "bf16" else "fp8_e4m3",
+            "data": "synthetic", "config": {"workload": f"shuffle_all_blocks_{w.name}", "num_blocks": nb,
+                                            "num_kv_heads": hkv, "bytes_per_call": moved,
+                                            "l2": "inputs larger than L2, no flush"},
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(gbs / peak, 4), "peak_kind": kind, "traffic": None,
+                         "algorithmic_bytes_per_launch": int(moved)},
+            "clocks": clocks, "gpu_launches": a.steps}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     a = _args()
+    if a.shuffle:
+        return run_shuffle(a, int(os.environ.get("LOCAL_RANK", 0)))
     if a.forward_layers > 0:
         return run_forward(a, si.config(a.config), int(os.environ.get("LOCAL_RANK", 0)))
     if a.kv_write:

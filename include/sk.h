@@ -209,6 +209,27 @@ int sk_reshape_and_cache(const void *key, const void *value, const int64_t *slot
                          int num_tokens, int num_kv_heads, int head_dim, void *kv_pages, int kv_dtype,
                          float k_scale, float v_scale, int num_blocks, int page_size, void *stream);
 
+/* Standard -> shuffled page conversion (vLLM RFC 59111, Proposed Change,
+ * Convert: the per-block view/permute that turns standard pages into ROCm
+ * AITER's shuffled pages).  With x = 16 / element size (8 for bf16, 16 for
+ * e4m3fn), for every block blk listed in block_ids (all num_blocks blocks when
+ * block_ids == NULL, num_ids then ignored), head h, token row n, dimension d:
+ *   k_shuf[blk][h][d / x][n][d % x] = kv_pages[blk][h][n][d]
+ *   v_shuf[blk][h][n / x][d][n % x] = kv_pages[blk][h][n][D + d]
+ * Other blocks of k_shuf and v_shuf are left alone.  An id outside
+ * [0, num_blocks) is skipped and sets SK_DEV_BAD_BLOCK in the device status.
+ *
+ * Layouts (device, caller-owned): kv_pages [num_blocks, num_kv_heads,
+ * page_size, 2*head_dim] (kv_dtype bf16 or e4m3fn, bytes copied as they are);
+ * k_shuf [num_blocks, num_kv_heads, head_dim / x, page_size, x];
+ * v_shuf [num_blocks, num_kv_heads, page_size / x, head_dim, x]; block_ids
+ * int32 [num_ids] or NULL.  All three arrays 16-byte aligned; head_dim 128,
+ * page_size 16.  Asynchronous on `stream`, no allocation, capture safe.
+ * Returns SK_OK or a negative sk_status. */
+int sk_std_to_shuffled(const void *kv_pages, int kv_dtype, const int32_t *block_ids, int num_ids,
+                       int num_blocks, int num_kv_heads, int head_dim, int page_size, void *k_shuf,
+                       void *v_shuf, void *stream);
+
 /* The whole attention call -- plan (use_plan != 0) or fixed split, split-KV
  * attention, merge -- without any device allocation, for callers that cannot
  * allocate: a host engine that owns all device memory through its own

@@ -69,6 +69,8 @@ def lib():
         L.sk_merge_segments.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, P, P, P]
         L.sk_reshape_and_cache.restype = i32
         L.sk_reshape_and_cache.argtypes = [P, P, P, i32, i32, i32, P, i32, f32, f32, i32, i32, P]
+        L.sk_std_to_shuffled.restype = i32
+        L.sk_std_to_shuffled.argtypes = [P, i32, P, i32, i32, i32, i32, i32, P, P, P]
         L.sk_get_device_status.restype = i32
         L.sk_get_device_status.argtypes = [P, i32]
         L.sk_paged_decode_attention_static.restype = i32
@@ -230,6 +232,27 @@ def sk_reshape_and_cache(key, value, slot_mapping, kv_pages, *, k_scale: float =
                                     _ptr(kv_pages), _kv_dtype(kv_pages), float(k_scale), float(v_scale),
                                     nb, page, _stream(stream))
     return _check(rc, "sk_reshape_and_cache")
+
+
+def sk_std_to_shuffled(kv_pages, k_shuf, v_shuf, block_ids=None, stream=None) -> int:
+    """Standard pages [NB, H, 16, 256] to shuffled K [NB, H, 128/x, 16, x] and
+    V [NB, H, 16/x, 128, x] (x = 16 / element size), for ``block_ids`` (int32)
+    or every block."""
+    import torch
+    _need(kv_pages, None, "kv_pages", 4)
+    _need(k_shuf, kv_pages.dtype, "k_shuf", 5)
+    _need(v_shuf, kv_pages.dtype, "v_shuf", 5)
+    if block_ids is not None:
+        _need(block_ids, torch.int32, "block_ids", 1)
+    nb, hkv, page, d2 = kv_pages.shape
+    d = d2 // 2
+    x = 16 // kv_pages.element_size()
+    if tuple(k_shuf.shape) != (nb, hkv, d // x, page, x) or tuple(v_shuf.shape) != (nb, hkv, page // x, d, x):
+        raise ValueError("k_shuf must be [NB, H, D/x, page, x] and v_shuf [NB, H, page/x, D, x]")
+    rc = lib().sk_std_to_shuffled(_ptr(kv_pages), _kv_dtype(kv_pages), _ptr(block_ids),
+                                  0 if block_ids is None else block_ids.numel(), nb, hkv, d, page,
+                                  _ptr(k_shuf), _ptr(v_shuf), _stream(stream))
+    return _check(rc, "sk_std_to_shuffled")
 
 
 def sk_static_scratch_bytes() -> int:

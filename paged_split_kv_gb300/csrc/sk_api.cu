@@ -372,6 +372,41 @@ int sk_reshape_and_cache(const void *key, const void *value, const int64_t *slot
     return SK_OK;
 }
 
+int sk_std_to_shuffled(const void *kv_pages, int kv_dtype, const int32_t *block_ids, int num_ids,
+                       int num_blocks, int num_kv_heads, int head_dim, int page_size, void *k_shuf,
+                       void *v_shuf, void *stream)
+{
+    if (num_blocks < 1 || num_kv_heads < 1 || (block_ids != nullptr && num_ids < 0))
+        return fail(SK_ERR_INVALID, "sk_std_to_shuffled: num_blocks=%d num_kv_heads=%d num_ids=%d", num_blocks,
+                    num_kv_heads, num_ids);
+    if (kv_dtype != SK_KV_BF16 && kv_dtype != SK_KV_FP8_E4M3)
+        return fail(SK_ERR_INVALID, "sk_std_to_shuffled: kv_dtype=%d", kv_dtype);
+    if (head_dim != kHeadDim)
+        return fail(SK_ERR_UNSUPPORTED, "sk_std_to_shuffled: head_dim=%d (only 128)", head_dim);
+    if (page_size != kPage)
+        return fail(SK_ERR_UNSUPPORTED, "sk_std_to_shuffled: page_size=%d (only 16)", page_size);
+    if (kv_pages == nullptr || k_shuf == nullptr || v_shuf == nullptr)
+        return fail(SK_ERR_INVALID, "sk_std_to_shuffled: null pointer argument");
+    if ((reinterpret_cast<uintptr_t>(kv_pages) | reinterpret_cast<uintptr_t>(k_shuf) |
+         reinterpret_cast<uintptr_t>(v_shuf)) & 15)
+        return fail(SK_ERR_INVALID, "sk_std_to_shuffled: kv_pages, k_shuf and v_shuf must be 16-byte aligned");
+    if (block_ids != nullptr && num_ids == 0)
+        return SK_OK;
+    int *status = nullptr;
+    int rc = status_ptr(&status);
+    if (rc != SK_OK)
+        return rc;
+    int sms = 0;
+    rc = sm_count(&sms);
+    if (rc != SK_OK)
+        return rc;
+    cudaError_t e = launch_std_to_shuffled(kv_pages, kv_dtype, block_ids, num_ids, num_blocks, num_kv_heads, k_shuf,
+                                           v_shuf, status, sms, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "shuffle kernel launch");
+    return SK_OK;
+}
+
 int sk_get_device_status(void *stream, int clear)
 {
     int *status = nullptr;

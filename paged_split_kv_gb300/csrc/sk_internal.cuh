@@ -114,6 +114,9 @@ cudaError_t launch_kv_write(const uint16_t *key, const uint16_t *value, const in
                             int num_tokens, int num_kv_heads, long long num_blocks, void *pages,
                             int kv_dtype, float k_scale, float v_scale, int *status, int num_sms,
                             cudaStream_t stream);
+cudaError_t launch_std_to_shuffled(const void *pages, int kv_dtype, const int32_t *ids, int num_ids,
+                                   long long num_blocks, int num_kv_heads, void *k_out, void *v_out,
+                                   int *status, int num_sms, cudaStream_t stream);
 cudaError_t launch_merge(const float *part_o, const float *part_m, const float *part_l,
                          const int32_t *tok_nseg, int fixed_nseg, int num_tokens, int H_q,
                          int seg_max, uint16_t *out, float *lse, cudaStream_t stream);

@@ -109,6 +109,22 @@ def test_kv_write_rejects_bad_arguments_without_cuda(sklib):
     assert call(nt=0, k=None, v=None, sm=None, pg=None) == 0   # nothing to write: no launch
 
 
+def test_shuffle_rejects_bad_arguments_without_cuda(sklib):
+    f = sklib.sk_std_to_shuffled
+
+    def call(pg=FAKE, dt=0, ids=None, n=0, nb=8, h=2, d=128, page=16, k=FAKE, v=FAKE):
+        return f(pg, dt, ids, n, nb, h, d, page, k, v, None)
+    assert call(d=64) == -3
+    assert call(page=8) == -3
+    assert call(dt=3) == -1
+    assert call(nb=0) == -1
+    assert call(h=0) == -1
+    assert call(ids=FAKE, n=-1) == -1
+    assert call(pg=None) == -1
+    assert call(v=ctypes.c_void_p(264)) == -1         # not 16-byte aligned
+    assert call(ids=FAKE, n=0) == 0                   # empty id list: no launch
+
+
 def test_python_binding_refuses_cpu_tensors(sklib):
     import torch
     import paged_split_kv_gb300 as sk
