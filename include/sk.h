@@ -122,9 +122,12 @@ long long sk_plan_launch_count(void);
 
 /* Split-KV paged attention (SGLang PR 39172, Modifications, second item).
  *
- * Grid: with a plan, (plan_capacity - 1) * num_kv_heads CTAs; CTA b takes
- * work item i = b / num_kv_heads and KV head h = b % num_kv_heads, reads
- * w = plan[1+i], and exits at once when w == -1.  Sequence s = w >> 16,
+ * Grid: with a plan, (plan_capacity - 1) * num_kv_heads * row_blocks CTAs,
+ * row_blocks = ceil(G * max_q_len / 64) when that exceeds 64 rows (else 1);
+ * CTA b takes row block b % row_blocks (rows [64 rb, 64 rb + 64) of the item)
+ * of work item i = (b / row_blocks) / num_kv_heads and KV head
+ * h = (b / row_blocks) % num_kv_heads, reads w = plan[1+i], and exits at once
+ * when w == -1 or the block is past the item's rows.  Sequence s = w >> 16,
  * segment g = w & 0xFFFF covers keys [g*T, min((g+1)*T, L_s)) with
  * T = plan[0] * sk_tile_tokens().  With plan == NULL the fixed split runs:
  * nseg = sk_fixed_nseg(bs, num_kv_heads, num_sms, seg_max) segments per

@@ -303,7 +303,12 @@ int sk_paged_decode_attn(const void *q, const void *kv_pages, int kv_dtype, floa
     p.score_scale_log2 = sm_scale * (kv_dtype == SK_KV_FP8_E4M3 ? k_scale : 1.f) * log2e;
     p.v_scale = kv_dtype == SK_KV_FP8_E4M3 ? v_scale : 1.f;
 
-    const int rp = attn_tc_rows(kv_dtype, p.G * max_q_len, num_blocks, num_kv_heads);
+    const long long rows_ll = (long long)p.G * max_q_len;
+    const int rows_max = rows_ll > 0x7FFFFFFFLL ? 0x7FFFFFFF : (int)rows_ll;
+    const int rp = attn_tc_rows(kv_dtype, rows_max, num_blocks, num_kv_heads);
+    p.row_blocks = rp > 0 ? (rows_max + rp - 1) / rp : 1;
+    if ((long long)num_items * num_kv_heads * p.row_blocks > 0x7FFFFFFFLL)
+        return fail(SK_ERR_INVALID, "sk_paged_decode_attn: grid too large");
     cudaError_t e = rp > 0 ? launch_attn_tc(p, kv_dtype, rp, static_cast<cudaStream_t>(stream))
                            : launch_attn_simt(p, kv_dtype, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)

@@ -101,7 +101,13 @@ struct Cfg {
     static constexpr int kOffQ = kOffVRing + kVBufs * kVBufBytes;
     static constexpr int kOffMisc = kOffQ + kQBytes;
     static constexpr int kSmemBytes = kOffMisc + kMiscBytes;
-    static constexpr int kTmemCols = ((kSBufs + 1) * RP <= 128) ? 128 : ((kSBufs + 1) * RP <= 256) ? 256 : 512;
+    // fp8 with up to 32 rows: Q's hi and lo terms are one operand of 2*RP rows, so one product
+    // per 32 dimensions gives S_hi | S_lo side by side (K read once), summed by the softmax
+    static constexpr bool kStackQ = FP8 && RP <= 32;
+    static constexpr int kSCols = kStackQ ? 2 * RP : RP;     // TMEM columns of one S buffer
+    static constexpr int kTmemNeed = kSBufs * kSCols + RP;
+    static constexpr int kTmemCols = kTmemNeed <= 128 ? 128 : kTmemNeed <= 256 ? 256 : 512;
+    static_assert(kTmemNeed <= 512, "TMEM columns");
     static constexpr uint32_t kTxBytes = FP8 ? 2 * kChunkRegion : 4 * kChunkRegion;   // bytes the TMA brings per stage
     static constexpr int kGroupBytes = FP8 ? 2048 : 4096;     // one 8-token group of the raw rows
     static constexpr int kPageBytes = 2 * kGroupBytes;        // one page (one TMA copy)
@@ -264,19 +270,27 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
     using C = Cfg<RP, FP8>;
     extern __shared__ __align__(1024) uint8_t smem[];
 
-    const int item = blockIdx.x / p.H_kv;
-    const int h = blockIdx.x - item * p.H_kv;
+    // CTA b: row block b % row_blocks (neighbouring CTAs share a work item's pages, so
+    // the later reads of a page find it in L2) of work item / KV head b / row_blocks.
+    const int ih = blockIdx.x / p.row_blocks;
+    const int rb = blockIdx.x - ih * p.row_blocks;
+    const int item = ih / p.H_kv;
+    const int h = ih - item * p.H_kv;
     WorkItem w;
     if (item >= p.num_items || !decode_work_item(p, item, w))
         return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int R = p.G * w.q_len;
+    const int R_all = p.G * w.q_len;                  // the item's rows, r = j * G + i
+    const int row0 = rb * RP;                         // this CTA's first row
+    const int R = R_all - row0 < RP ? R_all - row0 : RP;
     const uint32_t sbase = smem_u32(smem);
-    if (R > RP || (sbase & 1023u) != 0) {
-        if (threadIdx.x == 0)
-            atomicOr(p.status, R > RP ? SK_DEV_BAD_SEQ : SK_DEV_INTERNAL);
+    if (R_all > p.row_blocks * RP || (sbase & 1023u) != 0) {
+        if (threadIdx.x == 0 && rb == 0)
+            atomicOr(p.status, R_all > p.row_blocks * RP ? SK_DEV_BAD_SEQ : SK_DEV_INTERNAL);
         return;
     }
+    if (R <= 0)
+        return;                                       // a row block past this item's rows
 
     uint8_t *misc = smem + C::kOffMisc;
     const uint32_t mbase = sbase + C::kOffMisc;
@@ -338,7 +352,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             const int r = u >> 4, unit = u & 15;
             uint4 val = make_uint4(0u, 0u, 0u, 0u);
             if (r < R) {
-                const int j = r / p.G, i = r - j * p.G;
+                const int j = (row0 + r) / p.G, i = row0 + r - j * p.G;
                 const uint16_t *src = p.q + ((long long)(w.tok0 + j) * p.H_q + h * p.G + i) * kHeadDim + unit * 8;
                 val = __ldg(reinterpret_cast<const uint4 *>(src));
             }
@@ -353,7 +367,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
         for (int r = warp - 1; r < RP; r += kSetupThreads / 32) {
             float qv[4] = {0.f, 0.f, 0.f, 0.f};
             if (r < R) {
-                const int j = r / p.G, i = r - j * p.G;
+                const int j = (row0 + r) / p.G, i = row0 + r - j * p.G;
                 const uint2 raw = __ldg(reinterpret_cast<const uint2 *>(
                     p.q + ((long long)(w.tok0 + j) * p.H_q + h * p.G + i) * kHeadDim + lane * 4));
                 qv[0] = __uint_as_float(raw.x << 16);
@@ -402,7 +416,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
     tc_fence_after();
     }
     const uint32_t tmem = warp != 0 ? *reinterpret_cast<volatile uint32_t *>(misc + C::kTmemSlot) : 0u;
-    const uint32_t tmem_s0 = tmem, tmem_o = tmem + kSBufs * RP;
+    const uint32_t tmem_s0 = tmem, tmem_o = tmem + kSBufs * C::kSCols;
 
     if (warp == 0) {
         // ================================================================ TMA producer
@@ -459,7 +473,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
         // PV: V^T (MN-major, two 64-dim atoms) x P^T (MN-major), 8 steps of 16 tokens.
         // Descriptors are built once for stage 0 / Q; an operand elsewhere is the same descriptor
         // advanced by (byte offset >> 4) in its start-address field (shared addresses < 256 KB).
-        constexpr uint32_t idesc_qk = FP8 ? idesc_e4m3_f32(kTokTile, RP, 0, 0) : idesc_bf16_f32(kTokTile, RP, 0, 0);
+        constexpr uint32_t idesc_qk = FP8 ? idesc_e4m3_f32(kTokTile, C::kSCols, 0, 0) : idesc_bf16_f32(kTokTile, RP, 0, 0);
         constexpr uint32_t idesc_pv = FP8 ? idesc_f16_f32(kTokTile, RP, 1, 1) : idesc_bf16_f32(kTokTile, RP, 1, 1);
         const uint64_t d_kv0 = smem_desc_sw128(stage(0), 16, C::kGroupBytes);           // K-major K tile
         const uint64_t d_v0 = C::kVRing ? smem_desc_sw128(sbase + C::kOffVRing, C::kVDimStride, C::kVGroupStride)
@@ -492,7 +506,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                     break;
                 tc_fence_after();
                 const uint32_t so = (uint32_t)(st * C::kStageBytes);
-                if constexpr (FP8) {
+                if constexpr (C::kStackQ) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_f8_ss_warp(tmem_s0 + b * C::kSCols, adv(d_kv0, so + k * 32), adv(d_q0, k * 32), idesc_qk,
+                                       k > 0 ? 1u : 0u);
+                } else if constexpr (FP8) {
 #pragma unroll
                     for (int t = 0; t < 2; ++t)
 #pragma unroll
@@ -639,10 +658,22 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             ok = __all_sync(kFull, ok);          // tcgen05.ld is warp-collective
             if (ok) {
                 tc_fence_after();
+                const uint32_t s_col = tmem_s0 + sb * C::kSCols + r0 + lane_off;
 #pragma unroll
                 for (int c = 0; c < RH; c += kLd)
-                    tmem_ld32<kLd>(tmem_s0 + sb * RP + r0 + c + lane_off, x + c);
-                tmem_wait_ld();
+                    tmem_ld32<kLd>(s_col + c, x + c);
+                if constexpr (C::kStackQ) {
+                    float y[RH];
+#pragma unroll
+                    for (int c = 0; c < RH; c += kLd)
+                        tmem_ld32<kLd>(s_col + RP + c, y + c);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int r = 0; r < RH; ++r)
+                        x[r] += y[r];
+                } else {
+                    tmem_wait_ld();
+                }
             }
             tc_fence_before();
             __syncwarp();
@@ -652,10 +683,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             // tok < segment end and (causal) j' >= tok - (L - q_len)
             const int tok = k0 + j * kTokTile + tau;
             const int ahead = tok - causal_base;       // > 0: only query tokens j' >= ahead see this key
-            const int rmin = (p.causal && ahead > 0) ? ahead * p.G : 0;
+            const int rmin = ((p.causal && ahead > 0) ? ahead * p.G : 0) - row0;   // first local row that sees it
             bool need = false;
             // (padding rows r >= R have zero Q, so their scores are 0: harmless, and never written out)
-            if (ok && tok < k1 && rmin == 0) {
+            if (ok && tok < k1 && rmin <= 0) {
 #pragma unroll
                 for (int r = 0; r < RH; r += 4) {
                     const float4 t = *reinterpret_cast<const float4 *>(m_thr + r0 + r);
@@ -843,7 +874,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             named_bar_sync(bar_id, 128);
             const int r = r0 + tid;
             if (tid < RH && r < R) {
-                const int jq = r / p.G, i = r - jq * p.G;
+                const int jq = (row0 + r) / p.G, i = row0 + r - jq * p.G;
                 const long long slot = (long long)(w.tok0 + jq) * p.seg_max * p.H_q + (long long)w.g * p.H_q + h * p.G + i;
                 bulk_store_s2g(p.part_o + slot * kHeadDim, sbase + (uint32_t)(r * kHeadDim * 4), kHeadDim * 4);
                 bulk_commit_group();
@@ -893,21 +924,22 @@ cudaError_t launch_rp(const CUtensorMap &map, const AttnParams &p, cudaStream_t 
                                                       Cfg<RP, FP8>::kSmemBytes);
     if (attr_err != cudaSuccess)
         return attr_err;
-    const dim3 grid((unsigned)p.num_items * (unsigned)p.H_kv);
+    const dim3 grid((unsigned)p.num_items * (unsigned)p.H_kv * (unsigned)p.row_blocks);
     attn_tc_kernel<RP, FP8><<<grid, Cfg<RP, FP8>::kThreads, Cfg<RP, FP8>::kSmemBytes, stream>>>(map, p);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-// Rows per work item the tensor-core kernel takes (0: use the CUDA-core kernel).
+// Rows per CTA the tensor-core kernel takes (0: use the CUDA-core kernel); a work
+// item with more rows than that is split into row blocks, one CTA each.
 int attn_tc_rows(int kv_dtype, int rows_max, long long num_blocks, int H_kv)
 {
-    if ((kv_dtype != SK_KV_BF16 && kv_dtype != SK_KV_FP8_E4M3) || rows_max < 1 || rows_max > 64)
+    if ((kv_dtype != SK_KV_BF16 && kv_dtype != SK_KV_FP8_E4M3) || rows_max < 1 || rows_max > kMaxRowBlocks * 64)
         return 0;
     if (num_blocks * H_kv * 2 > 0x7FFFFFFFLL)
         return 0;
-    return rows_max <= 16 ? 16 : rows_max <= 32 ? 32 : 64;
+    return rows_max <= 16 ? 16 : rows_max <= 32 ? 32 : 64;     // above 64: row blocks of 64
 }
 
 cudaError_t launch_attn_tc(const AttnParams &p, int kv_dtype, int rp, cudaStream_t stream)

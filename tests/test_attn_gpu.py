@@ -36,11 +36,14 @@ def _small_problems():
         build_problem([300, 20], 2, 40, 4, seed=29),             # G = 10, rows not a power of two
         build_problem([700, 130, 2000, 9], [4, 4, 3, 4], 32, 2, kv_dtype=KV_FP8, k_scale=0.5, v_scale=0.25,
                       seed=30),                                  # fp8 with 64 rows per work item
+        build_problem([900, 33, 2000], [12, 5, 10], 16, 2, kv_dtype=KV_FP8, k_scale=0.5, v_scale=0.25,
+                      seed=33),                                  # fp8, up to 96 rows: two row blocks, the second partial
+        build_problem([600, 1500, 7], [12, 12, 3], 64, 4, seed=34),   # G 16 x q 12 = 192 rows: three row blocks
     ]
 
 
 @pytest.mark.parametrize("use_plan", [True, False])
-@pytest.mark.parametrize("k", range(10))
+@pytest.mark.parametrize("k", range(12))
 def test_small_problem_elementwise(k, use_plan):
     pr = _small_problems()[k]
     q, kv = problem_tensors(pr, DEV)
@@ -58,7 +61,7 @@ def test_small_problem_elementwise(k, use_plan):
     assert np.max(np.abs(lse[fin] - ref_lse[fin]), initial=0) <= 1e-3
 
 
-@pytest.mark.parametrize("k", [0, 2, 3, 6, 9])
+@pytest.mark.parametrize("k", [0, 2, 3, 6, 9, 10, 11])
 def test_small_problem_partials(k):
     """Every segment partial: o / l and m + log l are the segment's unique output
     and log-sum-exp; a row that sees no key of the segment has (-inf, 0, 0)."""
@@ -156,6 +159,30 @@ def test_full_workload_sampled_rows(idx):
     # the planned and the fixed split agree on the same inputs
     r2 = run_library(w, q, kv, use_plan=False)
     diff = (r2.out.float() - out).abs().max().item()
+    assert diff <= TOL_PLAN_VS_FIXED, diff
+
+
+@pytest.mark.parametrize("seq_len,bs,q,hq,hkv,kv_dtype", [
+    (8000, 16, 8, 32, 2, KV_BF16),      # 128 rows per work item: two row blocks
+    (20000, 8, 20, 32, 2, KV_BF16),     # 320 rows: five row blocks
+    (9000, 12, 12, 16, 2, KV_FP8),      # 96 rows, fp8
+])
+def test_many_rows_per_work_item_sampled(seq_len, bs, q, hq, hkv, kv_dtype):
+    """Work items with more than 64 query rows (long drafts with wide GQA groups)
+    run as row blocks of 64 on the tensor-core kernel: sampled rows vs the oracle,
+    and the planned split vs the fixed one."""
+    ks, vs = (0.5, 0.25) if kv_dtype == KV_FP8 else (1.0, 1.0)
+    w = si.make_workload(f"rows_{hq // hkv * q}", [seq_len] * bs, q, hq, hkv, seed=40 + q,
+                         kv_dtype=kv_dtype, k_scale=ks, v_scale=vs)
+    q_t, kv, r = _run_workload(w, torch.device(DEV))
+    assert r.status == 0
+    rng = np.random.default_rng(7 + q)
+    samples = oracle_sampled(w, q_t, kv, sorted(set(int(x) for x in rng.integers(0, bs, size=4))), 6, rng)
+    got = r.out.float().cpu().numpy()
+    worst = max(float(np.max(np.abs(got[t, h] - o))) for t, h, o, _ in samples)
+    assert worst <= tol_for(kv_dtype), worst
+    r2 = run_library(w, q_t, kv, use_plan=False)
+    diff = (r2.out.float() - r.out.float()).abs().max().item()
     assert diff <= TOL_PLAN_VS_FIXED, diff
 
 
