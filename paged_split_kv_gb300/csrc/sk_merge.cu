@@ -28,6 +28,7 @@ namespace {
 
 constexpr uint32_t kFull = 0xffffffffu;
 constexpr int kThreads = 128;
+constexpr int kPre = 8;            // o vectors a warp loads together with (m, l)
 
 __device__ __forceinline__ float seg_weight(float m, float l, float M)
 {
@@ -55,14 +56,25 @@ merge_kernel(const float *__restrict__ part_o, const float *__restrict__ part_m,
 
     float M = -CUDART_INF_F, lam = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    auto add = [&](int g, float wg) {
-        const float4 og = __ldg(reinterpret_cast<const float4 *>(part_o + (base + (long long)g * H_q) * kHeadDim) + lane);
+    auto load_o = [&](int g) {
+        return __ldg(reinterpret_cast<const float4 *>(part_o + (base + (long long)g * H_q) * kHeadDim) + lane);
+    };
+    auto fma4 = [&](const float4 og, float wg) {
         acc.x = fmaf(og.x, wg, acc.x);
         acc.y = fmaf(og.y, wg, acc.y);
         acc.z = fmaf(og.z, wg, acc.z);
         acc.w = fmaf(og.w, wg, acc.w);
     };
+    auto add = [&](int g, float wg) { fma4(load_o(g), wg); };
     if (n <= 64) {
+        // the first kPre of this warp's segments' o vectors are loaded with their (m, l),
+        // so a row with few segments costs one round trip to L2
+        float4 opre[kPre];
+#pragma unroll
+        for (int k = 0; k < kPre; ++k) {
+            const int g = sub + k * WPR;
+            opre[k] = g < n ? load_o(g) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
         float m0 = -CUDART_INF_F, l0 = 0.f, m1 = -CUDART_INF_F, l1 = 0.f;
         if (lane < n) {
             m0 = __ldg(part_m + base + (long long)lane * H_q);
@@ -80,8 +92,13 @@ merge_kernel(const float *__restrict__ part_o, const float *__restrict__ part_m,
             lam = l0 * w0 + l1 * w1;
             for (int o = 16; o > 0; o >>= 1)
                 lam += __shfl_xor_sync(kFull, lam, o);
+#pragma unroll
+            for (int k = 0; k < kPre; ++k) {
+                const int g = sub + k * WPR;           // g < 64; a zero vector when g >= n
+                fma4(opre[k], __shfl_sync(kFull, g < 32 ? w0 : w1, g & 31));
+            }
 #pragma unroll 8
-            for (int g = sub; g < n; g += WPR) {
+            for (int g = sub + kPre * WPR; g < n; g += WPR) {
                 const float wg = __shfl_sync(kFull, g < 32 ? w0 : w1, g & 31);
                 add(g, wg);
             }

@@ -71,6 +71,15 @@ plan_kernel(const int32_t *__restrict__ seq_lens, const int32_t *__restrict__ cu
         return cached ? (uint32_t)tiles_s[s] : (uint32_t)tiles_of(__ldg(seq_lens + s));
     };
 
+    // the query-token range of this thread's sequence, fetched with the lengths (one
+    // sequence per thread whenever bs <= 1024)
+    const bool one_seq = bs <= nthr;
+    int cu_a = 0, cu_b = 0;
+    if (one_seq && tid < bs) {
+        cu_a = __ldg(cu_q + tid);
+        cu_b = __ldg(cu_q + tid + 1);
+    }
+
     // 1. tile counts; largest, number of non-empty sequences, total
     long long my_max = 0, my_nonempty = 0, my_sum = 0;
     for (int s = tid; s < bs; s += nthr) {
@@ -179,7 +188,7 @@ plan_kernel(const int32_t *__restrict__ seq_lens, const int32_t *__restrict__ cu
                 plan[slot] = (int32_t)(((uint32_t)s << 16) | (uint32_t)g);
         }
         base += n;
-        const int a = __ldg(cu_q + s), b = __ldg(cu_q + s + 1);
+        const int a = one_seq ? cu_a : __ldg(cu_q + s), b = one_seq ? cu_b : __ldg(cu_q + s + 1);
         if (a < 0 || b < a || b > num_tokens) {
             atomicOr(status, SK_DEV_BAD_SEQ);
             continue;
