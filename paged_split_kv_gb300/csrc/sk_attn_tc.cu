@@ -2,26 +2,26 @@
 //
 // One CTA per (sequence, segment, KV head) work item, as in SGLang PR 39172
 // (Modifications, second item).  The GQA group's R = G * q_len query rows
-// (up to 64) share every K/V byte, so the two products of a 128-token tile are
-// dense contractions:
+// share every K/V byte, so the two products of a 128-token tile are dense
+// contractions:
 //     S^T [128 tokens x R] = K_tile [128 x 128 dims] . Q^T
 //     O^T [128 dims   x R] += V_tile^T [128 dims x 128 tokens] . P^T
 // Tokens and dimensions take the MMA's M = 128 and the query rows its N
-// (16, 32 or 64 columns).  S^T and O^T live in tensor memory (TMEM lane =
-// token for S, = dimension for O).
+// (16, 32 or 64 columns).  S^T (four buffers) and O^T live in tensor memory
+// (TMEM lane = token for S, = dimension for O).  An item with more than 64
+// rows is split into row blocks of 64, one CTA each, placed next to each other
+// so that they stream the same pages at about the same time (L2 serves the
+// repeats).
 //
 // Roles (352 threads; 480 with the fp8 converter warps):
-//   warp 0   TMA producer (8 pages per 128-token tile, 128-byte swizzle).
-//            bf16: 4 boxes of 64 elements x 16 rows per page land as
-//            [chunk][page][row][128 B], at once the K-major layout of K
-//            (chunks 0, 1) and the MN-major layout of V^T (chunks 2, 3).
-//            fp8: 2 boxes of 128 elements x 16 rows per page: K as
-//            [page][row][128 B] (K-major, one row is all 128 dims) and V raw.
-//            Pages past the segment end are zero-filled (out-of-bounds box),
-//            so they cost no HBM traffic.
-//   warp 1   allocates TMEM; issues the QK products (one elected lane).
-//   warp 10  issues the PV products (one elected lane).  Two issuing warps,
-//            each converged, keep a tile's 16 MMAs off one instruction stream.
+//   warp 0   TMA producer: one 4-D copy per page (8 per 128-token tile) into
+//            128-byte-swizzled atoms that are at once the K-major K operand
+//            and the MN-major V^T operand (layout below).  Pages past the
+//            segment end are out-of-bounds boxes: zero-filled, no HBM traffic.
+//            It starts as soon as the mbarriers exist.
+//   warp 1   allocates TMEM; issues the QK products.
+//   warp 10  issues the PV products.  Both issuers run converged and issue
+//            through one elected lane, so the descriptors stay warp-uniform.
 //   warps 2-9  softmax, two warpgroups: one thread per token of the tile (its
 //            TMEM lane); warps 2-5 take the first half of the query rows,
 //            warps 6-9 the second, each group on its own.
@@ -32,12 +32,15 @@
 //            Row sums are kept per thread and reduced once at the end.
 //            P^T is written over the tile's own K area, which QK no longer
 //            needs, so every stage carries its own P buffer.
+//   warps 11-14  (fp8, up to 32 rows) convert each landed tile's V codes to
+//            f16 into a two-buffer ring; with 64 rows the softmax threads
+//            convert one tile ahead into the stage instead.
 // fp8 pages: QK runs as kind::f8f6f4 on the e4m3 K codes as they arrive, with
 // Q split into two e4m3 terms (q * 2^e_r = hi + lo, a power-of-two scale per
-// row) accumulated into the same S; V rows are converted to f16 (exact for
-// e4m3), by warps 11-14 as each tile lands when a work item has up to 32 rows,
-// else by the softmax threads one tile ahead, and PV runs as kind::f16 with f16 P.  The
-// scales k_scale and v_scale are folded into the score scale and the output.
+// row): for up to 32 rows the two terms are one stacked operand (S_hi | S_lo,
+// added by the softmax), else two products into the same S.  V is exact in
+// f16, and PV runs as kind::f16 with f16 P.  The scales k_scale and v_scale are
+// folded into the score scale and the output.
 //
 // Every mbarrier wait is bounded (about two seconds); on expiry the CTA sets
 // SK_DEV_TIMEOUT in the device status word, waits (bounded) for its own copies
@@ -76,9 +79,11 @@ constexpr int kMaxSmem = 232448;                    // 227 KB per CTA
 // swizzle atom: token t's chunk c sits at (t / 8) * kGroupBytes + c * 1 KB +
 // (t % 8) * 128.  Every chunk is then a K-major (or MN-major) 128-byte-swizzled
 // operand over the 128 tokens whose 8-row groups are kGroupBytes apart.
-//   bf16: groups of 4 KB: chunks K 0-63 (later P^T), K 64-127, V 0-63, V 64-127
-//   fp8:  groups of 2 KB in [0,32K): chunks K codes (later P^T), V codes;
-//         [32K,48K) V f16 dims 0-63 | [48K,64K) V f16 dims 64-127 (8-token atoms 1 KB apart)
+//   bf16: 64 KB stages, groups of 4 KB: chunks K 0-63 (later P^T), K 64-127, V 0-63, V 64-127
+//   fp8:  groups of 2 KB: chunks K codes (later P^T), V codes.  With converter warps a
+//         stage is these 32 KB and the f16 V of a tile goes to a 32 KB ring buffer; else
+//         the stage is 64 KB and [32K,48K) | [48K,64K) hold the f16 V of dims 0-63 | 64-127.
+//         The f16 V is MN-major: 8-token atoms 1 KB apart, the two dimension halves 16 KB.
 template <int RP, bool FP8>
 struct Cfg {
     static_assert(RP == 16 || RP == 32 || RP == 64, "rows per work item: 16, 32 or 64");
@@ -309,10 +314,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
     auto bar_pfull = [&](int b) { return mbase + C::kBarPFull + 8 * b; };
     volatile int *pv_issued = reinterpret_cast<volatile int *>(misc + C::kPvIssued);
     const uint32_t bar_odone = mbase + C::kBarODone;
-    auto bar_vready = [&](int s) { return mbase + C::kBarVReady + 8 * s; };
+    auto bar_vready = [&](int v) { return mbase + C::kBarVReady + 8 * v; };
+    auto bar_vfree = [&](int v) { return mbase + C::kBarVFree + 8 * v; };
     const uint32_t q_s = sbase + C::kOffQ;
     auto stage = [&](int s) { return sbase + (uint32_t)(s * C::kStageBytes); };
-    auto bar_vfree = [&](int v) { return mbase + C::kBarVFree + 8 * v; };
 
     const int k0 = w.k0, k1 = w.k1;
     const int ntiles = k1 > k0 ? (k1 - k0 + kTokTile - 1) / kTokTile : 0;
@@ -343,77 +348,77 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
     constexpr int kSetupThreads = C::kThreads - 32;
     const int st_tid = threadIdx.x - 32;
     if (warp != 0) {
-    if (warp == 1) {
-        tmem_alloc(mbase + C::kTmemSlot, C::kTmemCols);
-        tmem_relinquish();
-    }
-    if constexpr (!FP8) {
-        for (int u = st_tid; u < RP * 16; u += kSetupThreads) {
-            const int r = u >> 4, unit = u & 15;
-            uint4 val = make_uint4(0u, 0u, 0u, 0u);
-            if (r < R) {
-                const int j = (row0 + r) / p.G, i = row0 + r - j * p.G;
-                const uint16_t *src = p.q + ((long long)(w.tok0 + j) * p.H_q + h * p.G + i) * kHeadDim + unit * 8;
-                val = __ldg(reinterpret_cast<const uint4 *>(src));
-            }
-            const int chunk = unit >> 3, uu = unit & 7;
-            st_shared_v4(q_s + chunk * (RP * 128) + r * 128 + ((uu ^ (r & 7)) << 4), val.x, val.y, val.z, val.w);
+        if (warp == 1) {
+            tmem_alloc(mbase + C::kTmemSlot, C::kTmemCols);
+            tmem_relinquish();
         }
-        for (int r = st_tid; r < RP; r += kSetupThreads)
-            crow[r] = p.score_scale_log2;
-    } else {
-        // Row r of Q scaled by 2^e (max |q| lands in [128, 256)), as two e4m3 terms hi + lo.
-        // One warp per row; lane l owns dimensions 4l..4l+3.
-        for (int r = warp - 1; r < RP; r += kSetupThreads / 32) {
-            float qv[4] = {0.f, 0.f, 0.f, 0.f};
-            if (r < R) {
-                const int j = (row0 + r) / p.G, i = row0 + r - j * p.G;
-                const uint2 raw = __ldg(reinterpret_cast<const uint2 *>(
-                    p.q + ((long long)(w.tok0 + j) * p.H_q + h * p.G + i) * kHeadDim + lane * 4));
-                qv[0] = __uint_as_float(raw.x << 16);
-                qv[1] = __uint_as_float(raw.x & 0xFFFF0000u);
-                qv[2] = __uint_as_float(raw.y << 16);
-                qv[3] = __uint_as_float(raw.y & 0xFFFF0000u);
+        if constexpr (!FP8) {
+            for (int u = st_tid; u < RP * 16; u += kSetupThreads) {
+                const int r = u >> 4, unit = u & 15;
+                uint4 val = make_uint4(0u, 0u, 0u, 0u);
+                if (r < R) {
+                    const int j = (row0 + r) / p.G, i = row0 + r - j * p.G;
+                    const uint16_t *src = p.q + ((long long)(w.tok0 + j) * p.H_q + h * p.G + i) * kHeadDim + unit * 8;
+                    val = __ldg(reinterpret_cast<const uint4 *>(src));
+                }
+                const int chunk = unit >> 3, uu = unit & 7;
+                st_shared_v4(q_s + chunk * (RP * 128) + r * 128 + ((uu ^ (r & 7)) << 4), val.x, val.y, val.z, val.w);
             }
-            float amax = fmaxf(fmaxf(fabsf(qv[0]), fabsf(qv[1])), fmaxf(fabsf(qv[2]), fabsf(qv[3])));
-            for (int o = 16; o > 0; o >>= 1)
-                amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
-            int e = 0;
-            if (amax > 0.f && amax < CUDART_INF_F) {
-                int ex;
-                frexpf(amax, &ex);               // amax in [2^(ex-1), 2^ex)
-                e = 8 - ex;                      // amax * 2^e in [128, 256)
-                e = e > 100 ? 100 : (e < -100 ? -100 : e);
-            }
-            float lo[4];
-            uint32_t hcodes = 0;
+            for (int r = st_tid; r < RP; r += kSetupThreads)
+                crow[r] = p.score_scale_log2;
+        } else {
+            // Row r of Q scaled by 2^e (max |q| lands in [128, 256)), as two e4m3 terms hi + lo.
+            // One warp per row; lane l owns dimensions 4l..4l+3.
+            for (int r = warp - 1; r < RP; r += kSetupThreads / 32) {
+                float qv[4] = {0.f, 0.f, 0.f, 0.f};
+                if (r < R) {
+                    const int j = (row0 + r) / p.G, i = row0 + r - j * p.G;
+                    const uint2 raw = __ldg(reinterpret_cast<const uint2 *>(
+                        p.q + ((long long)(w.tok0 + j) * p.H_q + h * p.G + i) * kHeadDim + lane * 4));
+                    qv[0] = __uint_as_float(raw.x << 16);
+                    qv[1] = __uint_as_float(raw.x & 0xFFFF0000u);
+                    qv[2] = __uint_as_float(raw.y << 16);
+                    qv[3] = __uint_as_float(raw.y & 0xFFFF0000u);
+                }
+                float amax = fmaxf(fmaxf(fabsf(qv[0]), fabsf(qv[1])), fmaxf(fabsf(qv[2]), fabsf(qv[3])));
+                for (int o = 16; o > 0; o >>= 1)
+                    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+                int e = 0;
+                if (amax > 0.f && amax < CUDART_INF_F) {
+                    int ex;
+                    frexpf(amax, &ex);               // amax in [2^(ex-1), 2^ex)
+                    e = 8 - ex;                      // amax * 2^e in [128, 256)
+                    e = e > 100 ? 100 : (e < -100 ? -100 : e);
+                }
+                float lo[4];
+                uint32_t hcodes = 0;
 #pragma unroll
-            for (int k = 0; k < 4; k += 2) {
-                const float x0 = ldexpf(qv[k], e), x1 = ldexpf(qv[k + 1], e);
-                const uint32_t hc = pack_e4m3x2(x0, x1);
-                const uint32_t hf = e4m3x2_to_f16x2(hc);              // the hi terms back, exactly
-                lo[k] = x0 - f16lo_to_float(hf);
-                lo[k + 1] = x1 - f16lo_to_float(hf >> 16);
-                hcodes |= (hc & 0xFFFFu) << (8 * k);
+                for (int k = 0; k < 4; k += 2) {
+                    const float x0 = ldexpf(qv[k], e), x1 = ldexpf(qv[k + 1], e);
+                    const uint32_t hc = pack_e4m3x2(x0, x1);
+                    const uint32_t hf = e4m3x2_to_f16x2(hc);              // the hi terms back, exactly
+                    lo[k] = x0 - f16lo_to_float(hf);
+                    lo[k + 1] = x1 - f16lo_to_float(hf >> 16);
+                    hcodes |= (hc & 0xFFFFu) << (8 * k);
+                }
+                const uint32_t lcodes = (pack_e4m3x2(lo[0], lo[1]) & 0xFFFFu) | ((pack_e4m3x2(lo[2], lo[3]) & 0xFFFFu) << 16);
+                // byte offset of dims 4l..4l+3 in the swizzled 128-byte row: 16-byte unit l/4, 4 bytes at (l%4)*4
+                const uint32_t off = (uint32_t)(r * 128 + ((((lane >> 2) ^ (r & 7)) << 4) | ((lane & 3) << 2)));
+                *reinterpret_cast<uint32_t *>(smem + C::kOffQ + off) = hcodes;
+                *reinterpret_cast<uint32_t *>(smem + C::kOffQ + RP * 128 + off) = lcodes;
+                if (lane == 0)
+                    crow[r] = p.score_scale_log2 * ldexpf(1.f, -e);
             }
-            const uint32_t lcodes = (pack_e4m3x2(lo[0], lo[1]) & 0xFFFFu) | ((pack_e4m3x2(lo[2], lo[3]) & 0xFFFFu) << 16);
-            // byte offset of dims 4l..4l+3 in the swizzled 128-byte row: 16-byte unit l/4, 4 bytes at (l%4)*4
-            const uint32_t off = (uint32_t)(r * 128 + ((((lane >> 2) ^ (r & 7)) << 4) | ((lane & 3) << 2)));
-            *reinterpret_cast<uint32_t *>(smem + C::kOffQ + off) = hcodes;
-            *reinterpret_cast<uint32_t *>(smem + C::kOffQ + RP * 128 + off) = lcodes;
-            if (lane == 0)
-                crow[r] = p.score_scale_log2 * ldexpf(1.f, -e);
         }
-    }
-    for (int r = st_tid; r < RP; r += kSetupThreads) {
-        m_run[r] = -CUDART_INF_F;
-        m_thr[r] = -CUDART_INF_F;
-        m_sub[r] = 0.f;
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    named_bar_sync(kSetupBar, kSetupThreads);
-    tc_fence_after();
+        for (int r = st_tid; r < RP; r += kSetupThreads) {
+            m_run[r] = -CUDART_INF_F;
+            m_thr[r] = -CUDART_INF_F;
+            m_sub[r] = 0.f;
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        named_bar_sync(kSetupBar, kSetupThreads);
+        tc_fence_after();
     }
     const uint32_t tmem = warp != 0 ? *reinterpret_cast<volatile uint32_t *>(misc + C::kTmemSlot) : 0u;
     const uint32_t tmem_s0 = tmem, tmem_o = tmem + kSBufs * C::kSCols;
@@ -469,7 +474,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
     } else if (warp == 1 || warp == kPvWarp) {
         // ================================================================ MMA issuers
         // Whole warps run these loops; one elected lane issues each MMA and commit.
-        // QK: bf16 kind::f16, 8 steps of 16 dims; fp8 kind::f8f6f4, 4 steps of 32 dims per Q term.
+        // QK: bf16 kind::f16, 8 steps of 16 dims; fp8 kind::f8f6f4, 4 steps of 32 dims, on the
+        // stacked hi|lo Q (up to 32 rows) or once per Q term.
         // PV: V^T (MN-major, two 64-dim atoms) x P^T (MN-major), 8 steps of 16 tokens.
         // Descriptors are built once for stage 0 / Q; an operand elsewhere is the same descriptor
         // advanced by (byte offset >> 4) in its start-address field (shared addresses < 256 KB).

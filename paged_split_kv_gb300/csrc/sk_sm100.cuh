@@ -50,20 +50,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
-// Non-blocking test: has the phase with the given parity completed?
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
 // Waits for the phase with the given parity to complete.  Gives up after
 // `limit` clock cycles, or when `abort` is not null and *abort becomes
 // nonzero; returns false then.
@@ -96,15 +82,6 @@ __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
-// ------------------------------------------------------------------ TMA
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
 }
 
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, int x, int y, int z, int w,
@@ -287,31 +264,6 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, int a_mn, in
            | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);   // A, B format 0: e4m3
 }
 
-// D[tmem] (+)= A[smem] * B[smem] with 8-bit operands (kind::f8f6f4); one thread issues.
-__device__ __forceinline__ void mma_f8_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                          uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// D[tmem] (+)= A[smem] * B[smem] with 16-bit operands (kind::f16: f16 or bf16 per the
-// instruction descriptor); one thread issues.
-__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                            uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
 // Warp-wide forms: every lane of a converged warp calls them with the same
 // operands; elect.sync picks one lane (the lowest, the same one every time),
 // which issues.  The operands stay warp-uniform, with no divergent branch.
@@ -339,6 +291,7 @@ __device__ __forceinline__ void mma_f8_ss_warp(uint32_t d_tmem, uint64_t a_desc,
         : "memory");
 }
 
+// Arrives on `bar` once every tcgen05.mma the elected lane issued so far has completed.
 __device__ __forceinline__ void mma_commit_warp(uint32_t bar)
 {
     asm volatile(
@@ -346,12 +299,6 @@ __device__ __forceinline__ void mma_commit_warp(uint32_t bar)
         "elect.sync _|e, 0xffffffff;\n\t"
         "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
         : "memory");
-}
-
-// Arrives on `bar` once every tcgen05.mma issued so far by this thread completes.
-__device__ __forceinline__ void mma_commit(uint32_t bar)
-{
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
 }  // namespace sm100
