@@ -148,8 +148,10 @@ long long sk_plan_launch_count(void);
  *   keys p <= L_s - q_s + j; otherwise all L_s keys.
  * Scores: sm_scale * k_scale * <q, k>; values are multiplied by v_scale (the
  *   two scales apply to fp8 pages only and are ignored for bf16).
- * max_q_len: an upper bound on every q_s; it sizes the kernel's row tile
- *   (rows per work item = G * q_s).
+ * max_q_len: an upper bound on every q_s (at least 1 when num_tokens > 0); it
+ *   sizes the kernel's row tile and row blocks (rows per work item = G * q_s).
+ *   G * max_q_len above 65536, or num_blocks * num_kv_heads above 2^30, is
+ *   SK_ERR_UNSUPPORTED.
  * Outputs (device, fp32): for every query token t of the item's sequence,
  *   every query head hq of KV head h, and the item's segment g:
  *     part_m[(t*seg_max + g)*num_q_heads + hq]  reference value m (score units)

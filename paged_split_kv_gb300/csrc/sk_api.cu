@@ -239,7 +239,8 @@ int sk_paged_decode_attn(const void *q, const void *kv_pages, int kv_dtype, floa
         return fail(SK_ERR_UNSUPPORTED, "sk_paged_decode_attn: page_size=%d (only 16)", page_size);
     if (bs < 1 || bs > 32767)
         return fail(SK_ERR_INVALID, "sk_paged_decode_attn: bs=%d outside [1, 32767]", bs);
-    if (num_tokens < 0 || max_q_len < 0 || block_table_stride < 1 || num_blocks < 1)
+    if (num_tokens < 0 || max_q_len < 0 || (num_tokens > 0 && max_q_len < 1) || block_table_stride < 1 ||
+        num_blocks < 1)
         return fail(SK_ERR_INVALID,
                     "sk_paged_decode_attn: num_tokens=%d max_q_len=%d stride=%d num_blocks=%d",
                     num_tokens, max_q_len, block_table_stride, num_blocks);
@@ -266,7 +267,16 @@ int sk_paged_decode_attn(const void *q, const void *kv_pages, int kv_dtype, floa
         fixed = sk_fixed_nseg(bs, num_kv_heads, num_sms, seg_max);
         num_items = bs * fixed;
     }
-    if ((long long)num_items * num_kv_heads > 0x7FFFFFFFLL)
+    const long long rows_ll = (long long)(num_q_heads / num_kv_heads) * max_q_len;
+    const int rows_max = rows_ll > 0x7FFFFFFFLL ? 0x7FFFFFFF : (int)rows_ll;
+    const int rp = attn_tc_rows(kv_dtype, rows_max, num_blocks, num_kv_heads);
+    if (num_tokens > 0 && rp == 0)
+        return fail(SK_ERR_UNSUPPORTED,
+                    "sk_paged_decode_attn: %d rows per work item (G * max_q_len) or %d blocks x %d heads "
+                    "exceed the kernel's limits (65536 rows; 2^30 block-heads)",
+                    rows_max, num_blocks, num_kv_heads);
+    const int row_blocks = rp > 0 ? (rows_max + rp - 1) / rp : 1;
+    if ((long long)num_items * num_kv_heads * row_blocks > 0x7FFFFFFFLL)
         return fail(SK_ERR_INVALID, "sk_paged_decode_attn: grid too large");
     if (num_tokens == 0)
         return SK_OK;
@@ -303,14 +313,8 @@ int sk_paged_decode_attn(const void *q, const void *kv_pages, int kv_dtype, floa
     p.score_scale_log2 = sm_scale * (kv_dtype == SK_KV_FP8_E4M3 ? k_scale : 1.f) * log2e;
     p.v_scale = kv_dtype == SK_KV_FP8_E4M3 ? v_scale : 1.f;
 
-    const long long rows_ll = (long long)p.G * max_q_len;
-    const int rows_max = rows_ll > 0x7FFFFFFFLL ? 0x7FFFFFFF : (int)rows_ll;
-    const int rp = attn_tc_rows(kv_dtype, rows_max, num_blocks, num_kv_heads);
-    p.row_blocks = rp > 0 ? (rows_max + rp - 1) / rp : 1;
-    if ((long long)num_items * num_kv_heads * p.row_blocks > 0x7FFFFFFFLL)
-        return fail(SK_ERR_INVALID, "sk_paged_decode_attn: grid too large");
-    cudaError_t e = rp > 0 ? launch_attn_tc(p, kv_dtype, rp, static_cast<cudaStream_t>(stream))
-                           : launch_attn_simt(p, kv_dtype, static_cast<cudaStream_t>(stream));
+    p.row_blocks = row_blocks;
+    cudaError_t e = launch_attn_tc(p, kv_dtype, rp, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return cuda_fail(e, "attention kernel launch");
     return SK_OK;

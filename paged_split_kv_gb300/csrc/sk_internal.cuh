@@ -29,7 +29,7 @@ struct AttnParams {
     int seg_max;
     int fixed_nseg;              // segments per sequence when plan == NULL
     int num_items;               // work items the grid covers (per KV head)
-    int row_blocks;              // CTAs per (work item, KV head), each taking up to 64 of its rows (tensor-core kernel)
+    int row_blocks;              // CTAs per (work item, KV head), each taking up to 64 of its rows
     int causal;
     float score_scale_log2;      // sm_scale * k_scale * log2(e)
     float v_scale;               // applied to o (1 for bf16)
@@ -106,11 +106,10 @@ int set_error(int code, const char *msg);
 cudaError_t launch_plan(const int32_t *seq_lens, const int32_t *cu_q, int bs, int num_tokens,
                         int budget, int seg_max, int32_t *plan, int plan_capacity,
                         int32_t *tok_nseg, int *status, cudaStream_t stream);
-cudaError_t launch_attn_simt(const AttnParams &p, int kv_dtype, cudaStream_t stream);
 // Tensor-core kernel: attn_tc_rows() gives the row tile (16, 32, 64) it would
-// use for a call, or 0 when the call goes to the CUDA-core kernel.
+// use for a call, or 0 when it cannot take the call.
 int attn_tc_rows(int kv_dtype, int rows_max, long long num_blocks, int H_kv);
-constexpr int kMaxRowBlocks = 64;   // rows per work item up to 64 * 64 on the tensor-core kernel
+constexpr int kMaxRowBlocks = 1024;   // rows per work item up to 1024 * 64
 cudaError_t launch_attn_tc(const AttnParams &p, int kv_dtype, int rp, cudaStream_t stream);
 cudaError_t launch_kv_write(const uint16_t *key, const uint16_t *value, const int64_t *slot_mapping,
                             int num_tokens, int num_kv_heads, long long num_blocks, void *pages,

@@ -81,6 +81,9 @@ def test_attention_rejects_bad_arguments_without_cuda(sklib):
     assert call(q=ctypes.c_void_p(264)) == -1          # not 16-byte aligned
     assert call(scale=0.0) == -1
     assert call(dt=1, ks=0.0) == -1
+    assert call(mq=0) == -1                            # tokens but no query length
+    assert call(mq=5000) == -3                         # 16 x 5000 rows per work item: past the kernel's limit
+    assert call(nb=1 << 30) == -3                      # 2^31 block-heads: past the tensor map
 
 
 def test_merge_rejects_bad_arguments_without_cuda(sklib):
