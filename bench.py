@@ -385,6 +385,7 @@ def run_sk(a, w, ws, rank, local):
 
     # end to end through the public call with host inputs (pinned), copies inside the region
     e2e = None
+    e2e_serving = None
     if a.e2e_steps > 0:
         host = {"q": q.cpu().pin_memory(), "kv": kv.cpu().pin_memory(), "bt": bt.cpu().pin_memory(),
                 "lens": lens.cpu().pin_memory(), "cu": cu.cpu().pin_memory()}
@@ -426,6 +427,7 @@ def run_sk(a, w, ws, rank, local):
         e2e = {"value": weak_scaling_tbps(w.kv_bytes, a.e2e_steps, ws, e2e_ms), "unit": "TB/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": e2e_ms / a.e2e_steps}
+        e2e_serving = _e2e_serving(a, w, sk, torch, dev, q, kv, bt, lens, cu, use_plan, nsm, ws, out)
         del host, dq, dkv
 
     if rank != 0:
@@ -478,12 +480,89 @@ def run_sk(a, w, ws, rank, local):
             "kv_tbps_attention_plus_merge": round(w.kv_bytes / (1e-3 * statistics.mean(
                 [x + y for x, y in zip(attn_ms, merge_ms)])) / 1e12, 4),
             "frac_of_8tbps_nominal": round(value / 8.0, 4),
-            "roofline": roofline, "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu,
+            "roofline": roofline, "clocks": clocks, "e2e": e2e, "e2e_serving": e2e_serving, "cpu_baseline": cpu,
             "gpu_launches": a.steps * (3 if use_plan else 2)}
     print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
     return 0
+
+
+def _e2e_serving(a, w, sk, torch, dev, q, kv, bt, lens, cu, use_plan, nsm, ws, ref_out):
+    """A serving step through the public calls with the K/V cache resident in HBM
+    (model state, as in a server): every step copies this step's inputs from pinned
+    host memory -- Q, the new tokens' K and V, their cache slots, seq_lens,
+    cu_seqlens_q and the block table -- writes the new K/V into the cache
+    (sk_reshape_and_cache), runs plan + attention + merge, and copies out and lse
+    back.  The new tokens' K/V are the cache's own rows, so the cache is unchanged.
+    The step runs as one captured CUDA graph."""
+    nt, hkv = w.num_tokens, w.num_kv_heads
+    slots = np.concatenate([
+        w.block_table[s, np.arange(int(w.seq_lens[s]) - int(w.q_lens[s]), int(w.seq_lens[s])) // w.page]
+        .astype(np.int64) * w.page + np.arange(int(w.seq_lens[s]) - int(w.q_lens[s]), int(w.seq_lens[s])) % w.page
+        for s in range(w.bs)]) if nt else np.zeros(0, np.int64)
+    st = torch.as_tensor(slots, device=dev)
+    blk, off = st // w.page, st % w.page
+    d = w.head_dim
+    k_new = kv[blk, :, off, :d].contiguous()
+    v_new = kv[blk, :, off, d:].contiguous()
+    if w.kv_dtype == si.KV_FP8:      # the step's K/V arrive in bf16 and are quantised by the write
+        k_new = (k_new.view(torch.float8_e4m3fn).float() * w.k_scale).to(torch.bfloat16)
+        v_new = (v_new.view(torch.float8_e4m3fn).float() * w.v_scale).to(torch.bfloat16)
+    host = {"q": q.cpu().pin_memory(), "k": k_new.cpu().pin_memory(), "v": v_new.cpu().pin_memory(),
+            "slots": st.cpu().pin_memory(), "lens": lens.cpu().pin_memory(), "cu": cu.cpu().pin_memory(),
+            "bt": bt.cpu().pin_memory()}
+    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    out_h = torch.empty((nt, w.num_q_heads, d), dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.empty((nt, w.num_q_heads), dtype=torch.float32).pin_memory()
+    wsp = {}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+
+    def step():
+        for k in host:
+            dev_in[k].copy_(host[k], non_blocking=True)
+        sk.sk_reshape_and_cache(dev_in["k"], dev_in["v"], dev_in["slots"], kv, k_scale=w.k_scale, v_scale=w.v_scale)
+        sk.sk_plan_cache_reset()
+        o, l = sk.paged_decode_attention(dev_in["q"], kv, dev_in["bt"], dev_in["lens"], dev_in["cu"],
+                                         max_q_len=w.max_q_len, sm_scale=w.sm_scale, num_sms=nsm,
+                                         k_scale=w.k_scale, v_scale=w.v_scale, causal=bool(w.causal),
+                                         seg_max=w.seg_max, use_plan=use_plan, workspace=wsp)
+        out_h.copy_(o, non_blocking=True)
+        lse_h.copy_(l, non_blocking=True)
+
+    # the step is captured once as a CUDA graph (the calls are capture safe) and replayed,
+    # as a server would run it: no per-call host work inside the timed region
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            step()
+        side.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            step()
+    torch.cuda.synchronize()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    steps = max(a.e2e_steps, 20)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        torch.distributed.barrier()
+    e0.record()
+    for _ in range(steps):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1), ws, dev)
+    if sk.sk_get_device_status(clear=True):
+        raise RuntimeError("device status set during the serving-step run")
+    assert torch.equal(out_h, ref_out.cpu()), "serving-step output differs from the device-resident run"
+    return {"value": weak_scaling_tbps(w.kv_bytes, steps, ws, ms), "unit": "TB/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": ms / steps,
+            "cache": "resident in HBM; each step writes its new tokens' K/V with sk_reshape_and_cache",
+            "launch": "one CUDA graph per step: H2D copies, KV write, plan, attention, merge, D2H copies"}
 
 
 def run_kv_write(a, local):
