@@ -39,11 +39,15 @@ def _small_problems():
         build_problem([900, 33, 2000], [12, 5, 10], 16, 2, kv_dtype=KV_FP8, k_scale=0.5, v_scale=0.25,
                       seed=33),                                  # fp8, up to 96 rows: two row blocks, the second partial
         build_problem([600, 1500, 7], [12, 12, 3], 64, 4, seed=34),   # G 16 x q 12 = 192 rows: three row blocks
+        build_problem([300, 2000, 1], [1, 4, 2], 8, 8, seed=35),      # G 1 (plain multi-head attention)
+        build_problem([500, 1500, 64], [3, 2, 1], 16, 4, kv_dtype=KV_FP8, k_scale=0.5, v_scale=0.25,
+                      seed=36),                                  # fp8, 4 KV heads, 12 rows: the 16-row tile
+        build_problem([400, 90, 1000], [10, 9, 1], 64, 4, causal=0, seed=37),   # not causal, 160 rows
     ]
 
 
 @pytest.mark.parametrize("use_plan", [True, False])
-@pytest.mark.parametrize("k", range(12))
+@pytest.mark.parametrize("k", range(15))
 def test_small_problem_elementwise(k, use_plan):
     pr = _small_problems()[k]
     q, kv = problem_tensors(pr, DEV)
@@ -61,7 +65,7 @@ def test_small_problem_elementwise(k, use_plan):
     assert np.max(np.abs(lse[fin] - ref_lse[fin]), initial=0) <= 1e-3
 
 
-@pytest.mark.parametrize("k", [0, 2, 3, 6, 9, 10, 11])
+@pytest.mark.parametrize("k", [0, 2, 3, 6, 9, 10, 11, 13, 14])
 def test_small_problem_partials(k):
     """Every segment partial: o / l and m + log l are the segment's unique output
     and log-sum-exp; a row that sees no key of the segment has (-inf, 0, 0)."""
