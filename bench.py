@@ -13,6 +13,15 @@ Metric: effective KV-read TB/s = K/V bytes of the batch / time per step
 
   python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--config I]
 
+Besides the contract's keys the line carries e2e_serving: the same step as a
+server runs it (cache resident in HBM, the step's new K/V written by
+sk_reshape_and_cache, inputs copied from pinned host memory, one CUDA graph).
+Other modes print a line of their own:
+
+  python bench.py --config I --forward-layers 15   # one plan + 15 layers, CUDA graph
+  python bench.py --kv-write bf16|fp8               # the KV write, 65536 tokens x 8 heads
+  python bench.py --shuffle bf16|fp8                # standard -> shuffled pages, a whole cache
+
 Under torchrun (N > 1) every rank runs its own copy of the batch on its own
 GPU (weak scaling: work items are independent, no collective on the data
 path); the timed region is bracketed by barriers and the max over ranks is
