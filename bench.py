@@ -70,6 +70,8 @@ def _args():
                          "(config 2's for bf16, config 4's for fp8)")
     ap.add_argument("--kv-write", choices=["bf16", "fp8"], default=None,
                     help="time the KV write step (65536 tokens x 8 KV heads) instead of the path")
+    ap.add_argument("--eager", action="store_true",
+                    help="launch every step from Python instead of replaying the steps as one CUDA graph")
     ap.add_argument("--fixed-split", action="store_true",
                     help="time the fixed split even when bs > 1 (bs == 1 always uses it, as the method does)")
     return ap.parse_args()
@@ -340,7 +342,15 @@ def run_sk(a, w, ws, rank, local):
     lse = torch.empty((nt, w.num_q_heads), dtype=torch.float32, device=dev)
     fixed = 0 if use_plan else sk.sk_fixed_nseg(w.bs, hkv, nsm, w.seg_max)
     flush = None if w.kv_bytes > 129e6 else torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream()
+    # The timed steps are captured once as a CUDA graph (every call is capture safe), with an
+    # event pair around each kernel recorded inside the graph, and replayed once: the device
+    # runs exactly the kernels of K eager steps, but the timing does not depend on how fast
+    # the host can issue ~15 calls a step.  --eager keeps the Python-launched loop.
+    try:
+        graph_events = not a.eager and torch.cuda.Event(enable_timing=True, external=True) is not None
+    except TypeError:                      # a PyTorch without graph-recorded events
+        graph_events = False
+    stream = torch.cuda.Stream(device=dev) if graph_events else torch.cuda.current_stream()
 
     def step(ev=None):
         if flush is not None:
@@ -365,19 +375,39 @@ def run_sk(a, w, ws, rank, local):
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
         sampler.start()
-    for _ in range(max(3, a.warmup)):
-        step()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+    torch.cuda.synchronize()
+    if graph_events:
+        evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)] for _ in range(a.steps)]
+        g_warm, g_timed = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g_warm, stream=stream):
+                for _ in range(max(3, a.warmup)):
+                    step()
+            with torch.cuda.graph(g_timed, stream=stream):
+                for i in range(a.steps):
+                    step(evs[i])
+        g_warm.replay()
+    else:
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(a.steps)]
+        for _ in range(max(3, a.warmup)):
+            step()
     torch.cuda.synchronize()
     status = sk.sk_get_device_status(clear=True)
     if status:
         raise RuntimeError(f"device status {status:#x} after warm-up")
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(a.steps)]
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    for i in range(a.steps):
-        step(evs[i])
+    if graph_events:
+        g_timed.replay()
+    else:
+        for i in range(a.steps):
+            step(evs[i])
     torch.cuda.synchronize()
     clocks = sampler.stop() if sampler else None
     if ws > 1:
@@ -490,7 +520,8 @@ def run_sk(a, w, ws, rank, local):
                 [x + y for x, y in zip(attn_ms, merge_ms)])) / 1e12, 4),
             "frac_of_8tbps_nominal": round(value / 8.0, 4),
             "roofline": roofline, "clocks": clocks, "e2e": e2e, "e2e_serving": e2e_serving, "cpu_baseline": cpu,
-            "gpu_launches": a.steps * (3 if use_plan else 2)}
+            "gpu_launches": a.steps * (3 if use_plan else 2),
+            "launch": "timed steps replayed as one CUDA graph" if graph_events else "eager, one Python call per kernel"}
     print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
