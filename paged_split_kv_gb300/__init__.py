@@ -2,12 +2,13 @@
 on GB300 (sm_103a).
 
 Argument marshalling only: every step of the path (plan, attention, merge)
-runs in the CUDA kernels of ``libsk.so``; torch supplies device memory and
-streams.  The functions carry the C names (``sk_build_plan``,
-``sk_paged_decode_attn``, ``sk_merge_segments``, ``sk_plan_cache_reset``) and
-take torch tensors; ``paged_decode_attention`` chains the three calls the
-way a serving step does.  If ``libsk.so`` has not been built, every call
-raises: there is no fallback.
+and the KV write and page conversion around it run in the CUDA kernels of
+``libsk.so``; torch supplies device memory and streams.  The functions carry
+the C names (``sk_build_plan``, ``sk_paged_decode_attn``,
+``sk_merge_segments``, ``sk_plan_cache_reset``, ``sk_reshape_and_cache``,
+``sk_std_to_shuffled``) and take torch tensors; ``paged_decode_attention``
+chains the three attention calls the way a serving step does.  If
+``libsk.so`` has not been built, every call raises: there is no fallback.
 """
 from __future__ import annotations
 
@@ -20,7 +21,8 @@ __all__ = [
     "SkError", "lib", "sk_tile_tokens", "sk_fixed_nseg", "sk_build_plan", "sk_plan_cache_reset",
     "sk_plan_launch_count", "sk_paged_decode_attn", "sk_merge_segments", "sk_get_device_status",
     "paged_decode_attention", "plan_capacity", "sk_paged_decode_attention_static",
-    "sk_static_scratch_bytes", "SK_OK", "SK_CACHED", "SK_KV_BF16", "SK_KV_FP8_E4M3",
+    "sk_static_scratch_bytes", "sk_reshape_and_cache", "sk_std_to_shuffled", "SK_OK", "SK_CACHED",
+    "SK_KV_BF16", "SK_KV_FP8_E4M3", "SK_DEV_BAD_BLOCK", "SK_DEV_BAD_SEQ", "SK_DEV_TIMEOUT",
 ]
 
 SK_OK = 0

@@ -937,8 +937,8 @@ cudaError_t launch_rp(const CUtensorMap &map, const AttnParams &p, cudaStream_t 
 
 }  // namespace
 
-// Rows per CTA the tensor-core kernel takes (0: use the CUDA-core kernel); a work
-// item with more rows than that is split into row blocks, one CTA each.
+// Rows per CTA the kernel takes (16, 32 or 64; 0 when it cannot take the call);
+// a work item with more rows than 64 is split into row blocks, one CTA each.
 int attn_tc_rows(int kv_dtype, int rows_max, long long num_blocks, int H_kv)
 {
     if ((kv_dtype != SK_KV_BF16 && kv_dtype != SK_KV_FP8_E4M3) || rows_max < 1 || rows_max > kMaxRowBlocks * 64)
