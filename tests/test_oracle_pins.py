@@ -359,3 +359,18 @@ def test_nan_in_unused_rows_never_reaches_results(oracle):
     pr = build_problem([17, 31, 1], [4, 1, 1], 8, 2, seed=14, garbage=np.nan)
     out, lse = oracle.attention(*pr.oracle_args())
     assert np.isfinite(out).all()
+
+
+# --------------------------------------------------------------------------- workload recipe
+
+def test_seeded_workloads_match_committed_configs():
+    """The seeded generator still produces the committed lengths and shapes."""
+    import sk_inputs as si
+    with open(os.path.join(os.path.dirname(__file__), "..", "sk_inputs", "configs.json")) as f:
+        committed = json.load(f)["workloads"]
+    for c in committed:
+        w = si.config(c["index"])
+        assert w.name == c["name"] and w.bs == c["bs"]
+        assert [int(x) for x in w.seq_lens] == c["seq_lens"]
+        assert [int(x) for x in w.q_lens] == c["q_lens"]
+        assert (w.num_q_heads, w.num_kv_heads, int(w.kv_bytes)) == (c["num_q_heads"], c["num_kv_heads"], c["kv_bytes"])
