@@ -283,14 +283,36 @@ def _peaks():
 ATTN_SOURCES = ("sk_attn_tc.cu", "sk_sm100.cuh", "sk_internal.cuh")
 
 
+def _strip_comments(src: str) -> str:
+    """C/C++ source without comments and blank lines (string literals are left alone)."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        if src.startswith("//", i):
+            i = src.find("\n", i)
+            i = n if i < 0 else i
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        elif src[i] == '"':
+            j = i + 1
+            while j < n and src[j] != '"':
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        else:
+            out.append(src[i])
+            i += 1
+    return "\n".join(line.rstrip() for line in "".join(out).splitlines() if line.strip())
+
+
 def _kernel_sources_sha():
-    """Short hash of the attention kernel's sources: an ncu traffic figure is
-    only reported while it was taken on exactly these sources."""
+    """Short hash of the attention kernel's code (comments and blank lines do not
+    count): an ncu traffic figure is only reported while it was taken on this code."""
     h = hashlib.sha256()
     for name in ATTN_SOURCES:
-        with open(os.path.join(ROOT, "paged_split_kv_gb300", "csrc", name), "rb") as fh:
+        with open(os.path.join(ROOT, "paged_split_kv_gb300", "csrc", name)) as fh:
             h.update(name.encode())
-            h.update(fh.read())
+            h.update(_strip_comments(fh.read()).encode())
     return h.hexdigest()[:16]
 
 
