@@ -13,7 +13,7 @@
 // so that they stream the same pages at about the same time (L2 serves the
 // repeats).
 //
-// Roles (352 threads; 480 with the fp8 converter warps):
+// Roles (352 threads):
 //   warp 0   TMA producer: one 4-D copy per page (8 per 128-token tile) into
 //            128-byte-swizzled atoms that are at once the K-major K operand
 //            and the MN-major V^T operand (layout below).  Pages past the
@@ -32,15 +32,14 @@
 //            Row sums are kept per thread and reduced once at the end.
 //            P^T is written over the tile's own K area, which QK no longer
 //            needs, so every stage carries its own P buffer.
-//   warps 11-14  (fp8, up to 32 rows) convert each landed tile's V codes to
-//            f16 into a two-buffer ring; with 64 rows the softmax threads
-//            convert one tile ahead into the stage instead.
-// fp8 pages: QK runs as kind::f8f6f4 on the e4m3 K codes as they arrive, with
-// Q split into two e4m3 terms (q * 2^e_r = hi + lo, a power-of-two scale per
-// row): for up to 32 rows the two terms are one stacked operand (S_hi | S_lo,
-// added by the softmax), else two products into the same S.  V is exact in
-// f16, and PV runs as kind::f16 with f16 P.  The scales k_scale and v_scale are
-// folded into the score scale and the output.
+// fp8 pages: both products run as kind::f8f6f4 on the e4m3 codes as they
+// arrive, so a stage is only the tile's 32 KB of codes and six stages fit.
+// QK splits Q into two e4m3 terms (q * 2^e_r = hi + lo, a power-of-two scale
+// per row): for up to 32 rows the two terms are one stacked operand (S_hi |
+// S_lo, added by the softmax), else two products into the same S.  PV splits
+// P the same way (p * 2^4 = hi + lo, about 8 significant bits), stacked as
+// 2R columns of P^T, so O^T holds O_hi | O_lo, added at the end.  The scales
+// k_scale and v_scale are folded into the score scale and the output.
 //
 // Every mbarrier wait is bounded (about two seconds); on expiry the CTA sets
 // SK_DEV_TIMEOUT in the device status word, waits (bounded) for its own copies
@@ -67,9 +66,8 @@ constexpr int kSoftmaxWarp0 = 2;
 constexpr int kSoftmaxGroups = 2;                   // warpgroups splitting the query rows
 constexpr int kSoftmaxWarps = 4 * kSoftmaxGroups;
 constexpr int kPvWarp = kSoftmaxWarp0 + kSoftmaxWarps;   // 10: issues the PV products
-constexpr int kConvWarp0 = kPvWarp + 1;             // 11-14: fp8 V converters, where present
+constexpr int kThreads = 32 * (kPvWarp + 1);        // 352
 constexpr int kSBufs = 4;                           // S^T buffers in TMEM (QK may run this far ahead of PV)
-constexpr float kRescaleLog2 = 8.0f;
 constexpr long long kWaitLimit = 4000000000LL;      // cycles (~2 s)
 constexpr uint32_t kFull = 0xffffffffu;
 constexpr int kMaxSmem = 232448;                    // 227 KB per CTA
@@ -80,47 +78,38 @@ constexpr int kMaxSmem = 232448;                    // 227 KB per CTA
 // (t % 8) * 128.  Every chunk is then a K-major (or MN-major) 128-byte-swizzled
 // operand over the 128 tokens whose 8-row groups are kGroupBytes apart.
 //   bf16: 64 KB stages, groups of 4 KB: chunks K 0-63 (later P^T), K 64-127, V 0-63, V 64-127
-//   fp8:  groups of 2 KB: chunks K codes (later P^T), V codes.  With converter warps a
-//         stage is these 32 KB and the f16 V of a tile goes to a 32 KB ring buffer; else
-//         the stage is 64 KB and [32K,48K) | [48K,64K) hold the f16 V of dims 0-63 | 64-127.
-//         The f16 V is MN-major: 8-token atoms 1 KB apart, the two dimension halves 16 KB.
+//   fp8:  32 KB stages, groups of 2 KB: chunks K codes (later P^T), V codes
 template <int RP, bool FP8>
 struct Cfg {
     static_assert(RP == 16 || RP == 32 || RP == 64, "rows per work item: 16, 32 or 64");
     static constexpr int kQBytes = 2 * RP * 128;            // bf16: two 64-column chunks; fp8: hi and lo terms
     static constexpr int kMiscBytes = 4096;
     static constexpr int kRH = RP / kSoftmaxGroups;          // rows per softmax warpgroup
-    // fp8 with up to 32 rows: a warpgroup of its own converts V, leaving the softmax warps
-    // P alone (with 64 rows the softmax needs the registers; it converts V itself)
-    static constexpr bool kConvWarps = FP8 && RP <= 32;
-    static constexpr int kThreads = 32 * (kConvWarp0 + (kConvWarps ? 4 : 0));   // 352 or 480
-    // With converter warps the f16 V lives in a ring of its own (freed by the PV that read
-    // it), so a stage holds only the 32 KB of codes and four stages fit; otherwise a stage
-    // is 64 KB (bf16 rows, or fp8 codes plus their f16 V).
-    static constexpr bool kVRing = kConvWarps;
-    static constexpr int kStageBytes = kVRing ? 2 * kChunkRegion : 4 * kChunkRegion;
-    static constexpr int kVBufBytes = 2 * kChunkRegion;      // f16 V of one tile
-    static constexpr int kVBufs = kVRing ? 2 : 0;
-    static constexpr int kStages = kVRing ? 4 : (3 * kStageBytes + kQBytes + kMiscBytes <= kMaxSmem) ? 3 : 2;
-    static constexpr int kOffVRing = kStages * kStageBytes;
-    static constexpr int kOffQ = kOffVRing + kVBufs * kVBufBytes;
+    static constexpr int kStageBytes = FP8 ? 2 * kChunkRegion : 4 * kChunkRegion;
+    static constexpr int kStagesFit = (kMaxSmem - kQBytes - kMiscBytes) / kStageBytes;
+    static constexpr int kStages = kStagesFit < 6 ? kStagesFit : 6;
+    static constexpr int kOffQ = kStages * kStageBytes;
     static constexpr int kOffMisc = kOffQ + kQBytes;
     static constexpr int kSmemBytes = kOffMisc + kMiscBytes;
     // fp8 with up to 32 rows: Q's hi and lo terms are one operand of 2*RP rows, so one product
     // per 32 dimensions gives S_hi | S_lo side by side (K read once), summed by the softmax
     static constexpr bool kStackQ = FP8 && RP <= 32;
     static constexpr int kSCols = kStackQ ? 2 * RP : RP;     // TMEM columns of one S buffer
-    static constexpr int kTmemNeed = kSBufs * kSCols + RP;
+    static constexpr int kOCols = FP8 ? 2 * RP : RP;         // O^T, or O_hi^T | O_lo^T
+    static constexpr int kTmemNeed = kSBufs * kSCols + kOCols;
     static constexpr int kTmemCols = kTmemNeed <= 128 ? 128 : kTmemNeed <= 256 ? 256 : 512;
     static_assert(kTmemNeed <= 512, "TMEM columns");
-    static constexpr uint32_t kTxBytes = FP8 ? 2 * kChunkRegion : 4 * kChunkRegion;   // bytes the TMA brings per stage
+    static constexpr uint32_t kTxBytes = kStageBytes;        // bytes the TMA brings per stage
     static constexpr int kGroupBytes = FP8 ? 2048 : 4096;     // one 8-token group of the raw rows
     static constexpr int kPageBytes = 2 * kGroupBytes;        // one page (one TMA copy)
-    // V operand: bf16 chunks 2-3 of the raw rows (atoms 1 KB apart along the dimensions,
-    // groups kGroupBytes apart), or the converted f16 (atoms 16 KB apart, groups 1 KB apart)
-    static constexpr int kOffV = FP8 ? 2 * kChunkRegion : 2048;   // within a stage (not used with kVRing)
-    static constexpr int kVDimStride = FP8 ? kChunkRegion : 1024;
-    static constexpr int kVGroupStride = FP8 ? 1024 : kGroupBytes;
+    // V^T operand: bf16 chunks 2-3 (two 64-dimension atoms 1 KB apart), fp8 chunk 1 (one atom)
+    static constexpr int kOffV = FP8 ? 1024 : 2048;
+    // Lazy running max: scores are exponentiated against the running max unless one beats it
+    // by 2^kThrLog2.  fp8 P is formed as p * 2^kPShift <= 2^8, which keeps the small
+    // probabilities clear of the e4m3 subnormals; the shift cancels in o / l and is undone
+    // in the partials.
+    static constexpr float kThrLog2 = FP8 ? 4.0f : 8.0f;
+    static constexpr int kPShift = FP8 ? 4 : 0;
     // misc area
     static constexpr int kBarFull = 0;                       // [kStages]
     static constexpr int kBarEmpty = 8 * kStages;            // [kStages]
@@ -128,22 +117,21 @@ struct Cfg {
     static constexpr int kBarSFree = kBarSFull + 8 * kSBufs; // [kSBufs]
     static constexpr int kBarPFull = kBarSFree + 8 * kSBufs; // [kSBufs], by S buffer
     static constexpr int kBarODone = kBarPFull + 8 * kSBufs; // committed once, after the last PV
-    static constexpr int kBarVReady = kBarODone + 8;         // [2]: V ring buffer filled (converter warps)
-    static constexpr int kBarVFree = kBarVReady + 16;        // [2]: V ring buffer read (its PV completed)
-    static constexpr int kTmemSlot = kBarVFree + 16;
+    static constexpr int kTmemSlot = kBarODone + 8;
     static constexpr int kAbort = kTmemSlot + 4;
     static constexpr int kPvIssued = kAbort + 4;             // int: PVs issued so far (written by the PV thread)
     static constexpr int kFlags = kPvIssued + 4;             // int[group][3][4]: per tile parity, then the epilogue
     static constexpr int kRed = 320;                         // float[group][4][32]
     static constexpr int kMrun = kRed + kSoftmaxGroups * 4 * 32 * 4;   // float[64] running max (log2 units)
     static constexpr int kMthr = kMrun + 64 * 4;             // float[64] running max + rescale threshold
-    static constexpr int kMsub = kMthr + 64 * 4;             // float[64] running max with -inf -> 0
+    static constexpr int kMsub = kMthr + 64 * 4;             // float[64] running max - kPShift, -inf -> 0
     static constexpr int kAlpha = kMsub + 64 * 4;            // float[64]; reused for the final l
     static constexpr int kCrow = kAlpha + 64 * 4;            // float[64] per-row score scale (log2 units)
+    static_assert(kStages >= 2, "shared memory");
     static_assert(kFlags + kSoftmaxGroups * 48 <= kRed, "misc area");
     static_assert(kCrow + 64 * 4 <= kMiscBytes, "misc area");
     static_assert(kSmemBytes <= kMaxSmem, "shared memory");
-    static_assert(kStages <= 8, "barrier area");
+    static_assert(RP * kHeadDim * 4 <= kStageBytes * kStages, "epilogue staging");
     static_assert((kOffQ % 1024) == 0 && (kMrun % 16) == 0 && (kMthr % 16) == 0 && (kMsub % 16) == 0 &&
                       (kCrow % 16) == 0,
                   "operand and vector alignment");
@@ -230,6 +218,21 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v)
     return r;
 }
 
+// Packed f16 pair -> packed e4m3 pair (low 16 bits), nearest even, saturated to +-448.
+__device__ __forceinline__ uint32_t f16x2_to_e4m3x2(uint32_t v)
+{
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(v));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t sub_f16x2(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
 // Low half of a packed f16 pair as float.
 __device__ __forceinline__ float f16lo_to_float(uint32_t v)
 {
@@ -244,32 +247,8 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
-// fp8: 16-byte unit u (dims 16u..16u+15) of token tau's V code row in stage `sb`
-// (TMA-swizzled) to f16, written as units 2(u%4), 2(u%4)+1 of the token's row in
-// the MN-major operand atom of dims [64(u/4), 64(u/4)+64) of the f16 V at `vdst`;
-// zeros if `zero`.
-template <int kGroupBytes>
-__device__ __forceinline__ void convert_v_unit(const uint8_t *sb, uint8_t *vdst, int tau, int u, bool zero)
-{
-    const uint8_t *vraw = sb + (tau >> 3) * kGroupBytes + 1024 + (tau & 7) * 128;
-    uint8_t *atom = vdst + (u >> 2) * kChunkRegion + (tau >> 3) * 1024 + (tau & 7) * 128;
-    uint4 cv = *reinterpret_cast<const uint4 *>(vraw + ((u ^ (tau & 7)) << 4));
-    if (zero)
-        cv = make_uint4(0u, 0u, 0u, 0u);
-    const uint32_t wv[4] = {cv.x, cv.y, cv.z, cv.w};
-    uint32_t hv[8];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        hv[2 * k] = e4m3x2_to_f16x2(wv[k]);
-        hv[2 * k + 1] = e4m3x2_to_f16x2(wv[k] >> 16);
-    }
-    const int u0 = 2 * (u & 3);
-    *reinterpret_cast<uint4 *>(atom + ((u0 ^ (tau & 7)) << 4)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-    *reinterpret_cast<uint4 *>(atom + (((u0 + 1) ^ (tau & 7)) << 4)) = make_uint4(hv[4], hv[5], hv[6], hv[7]);
-}
-
 template <int RP, bool FP8>
-__global__ void __launch_bounds__(Cfg<RP, FP8>::kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
 {
     using C = Cfg<RP, FP8>;
@@ -314,8 +293,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
     auto bar_pfull = [&](int b) { return mbase + C::kBarPFull + 8 * b; };
     volatile int *pv_issued = reinterpret_cast<volatile int *>(misc + C::kPvIssued);
     const uint32_t bar_odone = mbase + C::kBarODone;
-    auto bar_vready = [&](int v) { return mbase + C::kBarVReady + 8 * v; };
-    auto bar_vfree = [&](int v) { return mbase + C::kBarVFree + 8 * v; };
     const uint32_t q_s = sbase + C::kOffQ;
     auto stage = [&](int s) { return sbase + (uint32_t)(s * C::kStageBytes); };
 
@@ -327,10 +304,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(bar_full(s), 1);
             mbar_init(bar_empty(s), 1);
-        }
-        for (int v = 0; v < 2; ++v) {
-            mbar_init(bar_vready(v), 4);
-            mbar_init(bar_vfree(v), 1);
         }
         for (int b = 0; b < kSBufs; ++b) {
             mbar_init(bar_sfull(b), 1);
@@ -345,7 +318,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
     __syncthreads();   // barriers initialised: the producer starts its copies now
     // The other warps set up TMEM and Q meanwhile, then meet at a barrier of their own.
     constexpr uint32_t kSetupBar = 3;
-    constexpr int kSetupThreads = C::kThreads - 32;
+    constexpr int kSetupThreads = kThreads - 32;
     const int st_tid = threadIdx.x - 32;
     if (warp != 0) {
         if (warp == 1) {
@@ -476,14 +449,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
         // Whole warps run these loops; one elected lane issues each MMA and commit.
         // QK: bf16 kind::f16, 8 steps of 16 dims; fp8 kind::f8f6f4, 4 steps of 32 dims, on the
         // stacked hi|lo Q (up to 32 rows) or once per Q term.
-        // PV: V^T (MN-major, two 64-dim atoms) x P^T (MN-major), 8 steps of 16 tokens.
+        // PV: V^T (MN-major) x P^T (MN-major): bf16 kind::f16, 8 steps of 16 tokens; fp8
+        // kind::f8f6f4 on the V codes and the stacked hi|lo P, 4 steps of 32 tokens.
         // Descriptors are built once for stage 0 / Q; an operand elsewhere is the same descriptor
         // advanced by (byte offset >> 4) in its start-address field (shared addresses < 256 KB).
         constexpr uint32_t idesc_qk = FP8 ? idesc_e4m3_f32(kTokTile, C::kSCols, 0, 0) : idesc_bf16_f32(kTokTile, RP, 0, 0);
-        constexpr uint32_t idesc_pv = FP8 ? idesc_f16_f32(kTokTile, RP, 1, 1) : idesc_bf16_f32(kTokTile, RP, 1, 1);
+        constexpr uint32_t idesc_pv = FP8 ? idesc_e4m3_f32(kTokTile, C::kOCols, 1, 1) : idesc_bf16_f32(kTokTile, RP, 1, 1);
         const uint64_t d_kv0 = smem_desc_sw128(stage(0), 16, C::kGroupBytes);           // K-major K tile
-        const uint64_t d_v0 = C::kVRing ? smem_desc_sw128(sbase + C::kOffVRing, C::kVDimStride, C::kVGroupStride)
-                                        : smem_desc_sw128(stage(0) + C::kOffV, C::kVDimStride, C::kVGroupStride);  // MN-major V^T
+        const uint64_t d_v0 = smem_desc_sw128(stage(0) + C::kOffV, 1024, C::kGroupBytes); // MN-major V^T
         const uint64_t d_p0 = smem_desc_sw128(stage(0), 1024, C::kGroupBytes);          // MN-major P^T
         const uint64_t d_q0 = smem_desc_sw128(q_s, 16, 1024);                          // K-major Q
         auto adv = [](uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); };
@@ -548,21 +521,23 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             // stage (empty), which is also how the softmax learns that O holds tile i.
             for (int i = 0; i < ntiles && ok; ++i) {
                 ok = mbar_wait_bounded(bar_pfull(i % kSBufs), (i / kSBufs) & 1, abort_flag, kWaitLimit);
-                if (C::kVRing && ok)   // V(i) in f16; its phase cannot run ahead: V(i+2) needs PV(i) done
-                    ok = mbar_wait_bounded(bar_vready(i & 1), (i >> 1) & 1, abort_flag, kWaitLimit);
                 ok = __all_sync(kFull, ok);
                 if (!ok)
                     break;
                 tc_fence_after();
                 const uint32_t so = (uint32_t)((i % C::kStages) * C::kStageBytes);    // P^T over the dead K area
-                const uint32_t vo = C::kVRing ? (uint32_t)((i & 1) * C::kVBufBytes) : so;
+                if constexpr (FP8) {
 #pragma unroll
-                for (int k = 0; k < kPagesPerTile; ++k)
-                    mma_f16_ss_warp(tmem_o, adv(d_v0, vo + k * 2 * C::kVGroupStride), adv(d_p0, so + k * 2 * C::kGroupBytes),
-                                    idesc_pv, (i > 0 || k > 0) ? 1u : 0u);
+                    for (int k = 0; k < 4; ++k)
+                        mma_f8_ss_warp(tmem_o, adv(d_v0, so + k * 4 * C::kGroupBytes), adv(d_p0, so + k * 4 * C::kGroupBytes),
+                                       idesc_pv, (i > 0 || k > 0) ? 1u : 0u);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        mma_f16_ss_warp(tmem_o, adv(d_v0, so + k * 2 * C::kGroupBytes), adv(d_p0, so + k * 2 * C::kGroupBytes),
+                                        idesc_pv, (i > 0 || k > 0) ? 1u : 0u);
+                }
                 mma_commit_warp(bar_empty(i % C::kStages));
-                if constexpr (C::kVRing)
-                    mma_commit_warp(bar_vfree(i & 1));
                 last = i;
                 __syncwarp();
                 if (lane == 0)
@@ -580,38 +555,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             }
         }
         __syncwarp();
-    } else if (C::kConvWarps && warp >= kConvWarp0) {
-        // ================================================================ fp8 V converters
-        // One thread per token row of the tile: its 128 V codes to f16 in the MN-major operand
-        // layout of V ring buffer j % 2 as soon as the tile lands and PV(j-2) has read that
-        // buffer (rows past L in the last page become zeros); vready tells the PV issuer.
-        const int tau = (warp - kConvWarp0) * 32 + lane;
-        const int last_page_end = (w.L + kPage - 1) / kPage * kPage;
-        bool ok = true;
-        for (int j = 0; j < ntiles; ++j) {
-            const int st = j % C::kStages, vb = j & 1;
-            ok = mbar_wait_bounded(bar_full(st), (j / C::kStages) & 1, abort_flag, kWaitLimit);
-            if (ok && j >= 2)      // the buffer's previous tile, j-2, has been read by its PV
-                ok = mbar_wait_bounded(bar_vfree(vb), ((j >> 1) - 1) & 1, abort_flag, kWaitLimit);
-            ok = __all_sync(kFull, ok);
-            if (!ok)
-                break;
-            const int tokv = k0 + j * kTokTile + tau;
-            const bool zero = tokv >= w.L && tokv < last_page_end;
-            const uint8_t *sb = smem + st * C::kStageBytes;
-            uint8_t *vdst = smem + C::kOffVRing + vb * C::kVBufBytes;
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-                convert_v_unit<C::kGroupBytes>(sb, vdst, tau, u, zero);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(bar_vready(vb));
-        }
-        if (!ok && lane == 0) {
-            *abort_flag = 1;
-            atomicOr(p.status, SK_DEV_TIMEOUT);
-        }
     } else {
         // ================================================================ softmax warpgroups
         // Group g owns query rows [g*RH, (g+1)*RH): their S and O columns, running max, row
@@ -631,25 +574,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
         bool failed = false;
         volatile int *gflags = flags + wg * 12;
         float *gred = red + wg * (4 * 32);
-        // fp8: dims [64 wg, 64 wg + 64) of this token's V row of tile jt, e4m3 codes (TMA-swizzled)
-        // -> f16 in the MN-major operand layout (atom wg); rows past L become zeros.  The codes were
-        // written by the TMA: they are acquired through the stage's barrier, whose phase for tile jt
-        // cannot advance before tile jt's PV has run.  Returns false if that wait gave up.
-        auto convert_v = [&](int jt) -> bool {
-            const int stv = jt % C::kStages;
-            const bool got = mbar_wait_bounded(bar_full(stv), (jt / C::kStages) & 1, abort_flag, kWaitLimit);
-            const int tokv = k0 + jt * kTokTile + tau;
-            const bool zero = !got || (tokv >= w.L && tokv < last_page_end);
-#pragma unroll
-            for (int uu = 0; uu < 4; ++uu)
-                convert_v_unit<C::kGroupBytes>(smem + stv * C::kStageBytes, smem + stv * C::kStageBytes + C::kOffV, tau,
-                                               4 * wg + uu, zero);
-            return got;
-        };
-        if constexpr (FP8 && !C::kConvWarps) {
-            if (ntiles > 0 && !convert_v(0))
-                failed = true;
-        }
         float lsum[RH];
 #pragma unroll
         for (int r = 0; r < RH; ++r)
@@ -743,8 +667,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                     const float mn = fmaxf(mo, mt);
                     alpha_s[rg] = (mo == -CUDART_INF_F) ? 0.f : exp2f(mo - mn);
                     m_run[rg] = mn;
-                    m_thr[rg] = mn + kRescaleLog2;
-                    m_sub[rg] = mn == -CUDART_INF_F ? 0.f : mn;
+                    m_thr[rg] = mn + C::kThrLog2;
+                    m_sub[rg] = mn == -CUDART_INF_F ? 0.f : mn - (float)C::kPShift;
                 }
                 named_bar_sync(bar_id, 128);
 #pragma unroll
@@ -761,14 +685,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                     if (okp) {
                         tc_fence_after();
 #pragma unroll
-                        for (int c = 0; c < RH; c += kLd) {
-                            float o[kLd];
-                            tmem_ld32<kLd>(tmem_o + r0 + c + lane_off, o);
-                            tmem_wait_ld();
+                        for (int half = 0; half < C::kOCols / RP; ++half) {
 #pragma unroll
-                            for (int r = 0; r < kLd; ++r)
-                                o[r] *= alpha_s[r0 + c + r];
-                            tmem_st32<kLd>(tmem_o + r0 + c + lane_off, o);
+                            for (int c = 0; c < RH; c += kLd) {
+                                float o[kLd];
+                                const uint32_t col = tmem_o + half * RP + r0 + c + lane_off;
+                                tmem_ld32<kLd>(col, o);
+                                tmem_wait_ld();
+#pragma unroll
+                                for (int r = 0; r < kLd; ++r)
+                                    o[r] *= alpha_s[r0 + c + r];
+                                tmem_st32<kLd>(col, o);
+                            }
                         }
                         tmem_wait_st();
                     } else {
@@ -779,7 +707,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             if (!failed) {
                 // probabilities against the running max (masked entries are -inf -> 0), written as
                 // this token's row of P^T over the tile's K area, which QK(j) no longer needs:
-                // MN-major, 128-byte swizzle, 16-byte unit u of row tau stored at u ^ (tau % 8)
+                // MN-major, 128-byte swizzle, 16-byte unit u of row tau stored at u ^ (tau % 8).
+                // bf16: row r at bytes [2r, 2r + 2).  fp8: p * 2^kPShift = hi + lo, two e4m3 codes
+                // at bytes r and RP + r (the lo term is the f16 residual, which is exact).
                 uint8_t *prow = smem + st * C::kStageBytes + (tau >> 3) * C::kGroupBytes + (tau & 7) * 128;
 #pragma unroll
                 for (int u = 0; u < RH / 8; ++u) {
@@ -796,16 +726,30 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                         lsum[r + 1] += p1;
                         pk[e] = FP8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
                     }
-                    const int ug = r0 / 8 + u;                 // unit of the row
-                    *reinterpret_cast<uint4 *>(prow + ((ug ^ (tau & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                }
-                const bool tail_row = tok >= w.L && tok < last_page_end;   // past L in the last page: anything
-                if (!FP8 && tail_row) {
-                    // V dims [64 wg, 64 wg + 64) of this row: chunk 2 + wg
-                    uint8_t *vrow = smem + st * C::kStageBytes + C::kOffV + wg * 1024 + (tau >> 3) * C::kGroupBytes +
-                                    (tau & 7) * 128;
+                    if constexpr (FP8) {
+                        uint32_t hc[4], lc[4];
 #pragma unroll
-                    for (int u = 0; u < 8; ++u)
+                        for (int e = 0; e < 4; ++e) {
+                            hc[e] = f16x2_to_e4m3x2(pk[e]);
+                            lc[e] = f16x2_to_e4m3x2(sub_f16x2(pk[e], e4m3x2_to_f16x2(hc[e])));
+                        }
+                        const int bh = r0 + 8 * u, bl = RP + r0 + 8 * u;     // byte of the first row
+                        *reinterpret_cast<uint2 *>(prow + (((bh >> 4) ^ (tau & 7)) << 4) + (bh & 15)) =
+                            make_uint2(hc[0] | (hc[1] << 16), hc[2] | (hc[3] << 16));
+                        *reinterpret_cast<uint2 *>(prow + (((bl >> 4) ^ (tau & 7)) << 4) + (bl & 15)) =
+                            make_uint2(lc[0] | (lc[1] << 16), lc[2] | (lc[3] << 16));
+                    } else {
+                        const int ug = r0 / 8 + u;                 // unit of the row
+                        *reinterpret_cast<uint4 *>(prow + ((ug ^ (tau & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    }
+                }
+                if (tok >= w.L && tok < last_page_end) {
+                    // past L in the last page the row holds anything (0 * NaN would reach O): this
+                    // group's half of the token's V row becomes zeros (bf16 chunk 2 + wg, fp8 64 bytes)
+                    uint8_t *vrow = smem + st * C::kStageBytes + C::kOffV + (tau >> 3) * C::kGroupBytes + (tau & 7) * 128 +
+                                    wg * (FP8 ? 64 : 1024);
+#pragma unroll
+                    for (int u = 0; u < (FP8 ? 4 : 8); ++u)
                         *reinterpret_cast<uint4 *>(vrow + u * 16) = make_uint4(0u, 0u, 0u, 0u);
                 }
                 fence_proxy_async_smem();
@@ -814,10 +758,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(bar_pfull(sb));
-            // fp8: the next tile's V conversion fills the wait for its S (its stage is free once it
-            // has landed); the fence before that tile's P_full publishes it to the tensor core
-            if (FP8 && !C::kConvWarps && !failed && j + 1 < ntiles && !convert_v(j + 1))
-                failed = true;
             if (failed) {
                 // the next tile's group decision propagates the failure
                 *abort_flag = 1;
@@ -859,12 +799,22 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             if (ntiles > 0)
                 tc_fence_after();
             float *orow = reinterpret_cast<float *>(smem);
+            const float o_scale = p.v_scale * (1.0f / (float)(1 << C::kPShift));
 #pragma unroll
             for (int c = 0; c < RH; c += kLd) {
                 float o[kLd];
                 if (ntiles > 0) {
                     tmem_ld32<kLd>(tmem_o + r0 + c + lane_off, o);
-                    tmem_wait_ld();
+                    if constexpr (FP8) {
+                        float o2[kLd];
+                        tmem_ld32<kLd>(tmem_o + RP + r0 + c + lane_off, o2);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int r = 0; r < kLd; ++r)
+                            o[r] += o2[r];
+                    } else {
+                        tmem_wait_ld();
+                    }
                 } else {
 #pragma unroll
                     for (int r = 0; r < kLd; ++r)
@@ -873,7 +823,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
 #pragma unroll
                 for (int rr = 0; rr < kLd; ++rr) {
                     const int r = r0 + c + rr;
-                    orow[r * kHeadDim + tau] = alpha_s[r] > 0.f ? o[rr] * p.v_scale : 0.f;
+                    orow[r * kHeadDim + tau] = alpha_s[r] > 0.f ? o[rr] * o_scale : 0.f;
                 }
             }
             fence_proxy_async_smem();
@@ -884,7 +834,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                 const long long slot = (long long)(w.tok0 + jq) * p.seg_max * p.H_q + (long long)w.g * p.H_q + h * p.G + i;
                 bulk_store_s2g(p.part_o + slot * kHeadDim, sbase + (uint32_t)(r * kHeadDim * 4), kHeadDim * 4);
                 bulk_commit_group();
-                const float l = alpha_s[r];
+                const float l = alpha_s[r] * (1.0f / (float)(1 << C::kPShift));
                 p.part_m[slot] = l > 0.f ? m_run[r] * 0.69314718055994531f : -CUDART_INF_F;
                 p.part_l[slot] = l;
                 bulk_wait_reads();
@@ -931,7 +881,7 @@ cudaError_t launch_rp(const CUtensorMap &map, const AttnParams &p, cudaStream_t 
     if (attr_err != cudaSuccess)
         return attr_err;
     const dim3 grid((unsigned)p.num_items * (unsigned)p.H_kv * (unsigned)p.row_blocks);
-    attn_tc_kernel<RP, FP8><<<grid, Cfg<RP, FP8>::kThreads, Cfg<RP, FP8>::kSmemBytes, stream>>>(map, p);
+    attn_tc_kernel<RP, FP8><<<grid, kThreads, Cfg<RP, FP8>::kSmemBytes, stream>>>(map, p);
     return cudaGetLastError();
 }
 
