@@ -59,15 +59,13 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kTokTile = 128;                       // tokens per tile (MMA M)
-constexpr int kPagesPerTile = kTokTile / kPage;     // 8
+constexpr int kTokTile = 128;                       // tokens per MMA (M)
 constexpr int kChunkRegion = kTokTile * 128;        // 16 KB: 128 token rows of 128 B
 constexpr int kSoftmaxWarp0 = 2;
 constexpr int kSoftmaxGroups = 2;                   // warpgroups splitting the query rows
 constexpr int kSoftmaxWarps = 4 * kSoftmaxGroups;
 constexpr int kPvWarp = kSoftmaxWarp0 + kSoftmaxWarps;   // 10: issues the PV products
 constexpr int kThreads = 32 * (kPvWarp + 1);        // 352
-constexpr int kSBufs = 4;                           // S^T buffers in TMEM (QK may run this far ahead of PV)
 constexpr long long kWaitLimit = 4000000000LL;      // cycles (~2 s)
 constexpr uint32_t kFull = 0xffffffffu;
 constexpr int kMaxSmem = 232448;                    // 227 KB per CTA
@@ -76,16 +74,25 @@ constexpr int kMaxSmem = 232448;                    // 227 KB per CTA
 // groups, each group as its 128-byte chunks of the row, each chunk an 8 x 128 B
 // swizzle atom: token t's chunk c sits at (t / 8) * kGroupBytes + c * 1 KB +
 // (t % 8) * 128.  Every chunk is then a K-major (or MN-major) 128-byte-swizzled
-// operand over the 128 tokens whose 8-row groups are kGroupBytes apart.
-//   bf16: 64 KB stages, groups of 4 KB: chunks K 0-63 (later P^T), K 64-127, V 0-63, V 64-127
-//   fp8:  32 KB stages, groups of 2 KB: chunks K codes (later P^T), V codes
+// operand over 128 tokens whose 8-row groups are kGroupBytes apart.
+//   bf16: 128-token tiles, 64 KB stages, groups of 4 KB: chunks K 0-63 (later P^T),
+//         K 64-127, V 0-63, V 64-127
+//   fp8:  groups of 2 KB: chunks K codes (later P^T), V codes.  Up to 32 rows a tile is
+//         256 tokens (64 KB, two 128-token halves 32 KB apart), so the softmax's fixed
+//         cost per tile is spread over as many bytes as a bf16 tile; with 64 rows it is
+//         128 tokens (32 KB).
 template <int RP, bool FP8>
 struct Cfg {
     static_assert(RP == 16 || RP == 32 || RP == 64, "rows per work item: 16, 32 or 64");
     static constexpr int kQBytes = 2 * RP * 128;            // bf16: two 64-column chunks; fp8: hi and lo terms
     static constexpr int kMiscBytes = 4096;
     static constexpr int kRH = RP / kSoftmaxGroups;          // rows per softmax warpgroup
-    static constexpr int kStageBytes = FP8 ? 2 * kChunkRegion : 4 * kChunkRegion;
+    static constexpr int kTile = (FP8 && RP <= 32) ? 256 : 128;   // tokens per tile
+    static constexpr int kHalves = kTile / kTokTile;          // 128-token MMAs per tile
+    static constexpr int kPagesPerTile = kTile / kPage;       // TMA copies per tile (<= 32 lanes)
+    static constexpr int kStageBytes = kTile * (FP8 ? 256 : 512);
+    // S^T buffers in TMEM: QK may run this many tiles ahead of PV
+    static constexpr int kSBufs = kHalves == 2 ? 2 : 4;
     static constexpr int kStagesFit = (kMaxSmem - kQBytes - kMiscBytes) / kStageBytes;
     static constexpr int kStages = kStagesFit < 6 ? kStagesFit : 6;
     static constexpr int kOffQ = kStages * kStageBytes;
@@ -96,7 +103,8 @@ struct Cfg {
     static constexpr bool kStackQ = FP8 && RP <= 32;
     static constexpr int kSCols = kStackQ ? 2 * RP : RP;     // TMEM columns of one S buffer
     static constexpr int kOCols = FP8 ? 2 * RP : RP;         // O^T, or O_hi^T | O_lo^T
-    static constexpr int kTmemNeed = kSBufs * kSCols + kOCols;
+    static constexpr int kSBufCols = kHalves * kSCols;       // one S buffer: a tile's halves side by side
+    static constexpr int kTmemNeed = kSBufs * kSBufCols + kOCols;
     static constexpr int kTmemCols = kTmemNeed <= 128 ? 128 : kTmemNeed <= 256 ? 256 : 512;
     static_assert(kTmemNeed <= 512, "TMEM columns");
     static constexpr uint32_t kTxBytes = kStageBytes;        // bytes the TMA brings per stage
@@ -297,7 +305,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
     auto stage = [&](int s) { return sbase + (uint32_t)(s * C::kStageBytes); };
 
     const int k0 = w.k0, k1 = w.k1;
-    const int ntiles = k1 > k0 ? (k1 - k0 + kTokTile - 1) / kTokTile : 0;
+    const int ntiles = k1 > k0 ? (k1 - k0 + C::kTile - 1) / C::kTile : 0;
 
     // ---- set-up: barriers, TMEM, Q in shared memory (K-major, 128-byte swizzle)
     if (threadIdx.x == 0) {
@@ -305,7 +313,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             mbar_init(bar_full(s), 1);
             mbar_init(bar_empty(s), 1);
         }
-        for (int b = 0; b < kSBufs; ++b) {
+        for (int b = 0; b < C::kSBufs; ++b) {
             mbar_init(bar_sfull(b), 1);
             mbar_init(bar_sfree(b), kSoftmaxWarps);
             mbar_init(bar_pfull(b), kSoftmaxWarps);
@@ -394,7 +402,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
         tc_fence_after();
     }
     const uint32_t tmem = warp != 0 ? *reinterpret_cast<volatile uint32_t *>(misc + C::kTmemSlot) : 0u;
-    const uint32_t tmem_s0 = tmem, tmem_o = tmem + kSBufs * C::kSCols;
+    const uint32_t tmem_s0 = tmem, tmem_o = tmem + C::kSBufs * C::kSBufCols;
 
     if (warp == 0) {
         // ================================================================ TMA producer
@@ -404,7 +412,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
         const int page_end = (k1 + kPage - 1) / kPage;
         const int32_t *bt_row = p.block_table + (long long)w.s * p.bt_stride;
         int blk_next = -1;
-        if (lane < kPagesPerTile && page0 + lane < page_end)
+        if (lane < C::kPagesPerTile && page0 + lane < page_end)
             blk_next = __ldg(bt_row + page0 + lane);
         int issued = 0;
         bool ok = true;
@@ -416,15 +424,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             if (!ok)
                 break;
             const int blk = blk_next;
-            const int pg = page0 + j * kPagesPerTile + lane;
-            const int pg_next = pg + kPagesPerTile;
+            const int pg = page0 + j * C::kPagesPerTile + lane;
+            const int pg_next = pg + C::kPagesPerTile;
             blk_next = -1;
-            if (lane < kPagesPerTile && j + 1 < ntiles && pg_next < page_end)
+            if (lane < C::kPagesPerTile && j + 1 < ntiles && pg_next < page_end)
                 blk_next = __ldg(bt_row + pg_next);
             if (lane == 0)
                 mbar_arrive_expect_tx(bar_full(st), C::kTxBytes);
             __syncwarp();
-            if (lane < kPagesPerTile) {
+            if (lane < C::kPagesPerTile) {
                 int grp = -2;                         // whole box out of bounds: zero fill
                 if (pg < page_end) {
                     if (blk >= 0 && blk < p.num_blocks)
@@ -467,13 +475,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             // is issued.  The last condition keeps barrier phases unambiguous: P_full[b] cannot
             // run a full round of buffers ahead of its PV.
             for (int j = 0; j < ntiles && ok; ++j) {
-                const int st = j % C::kStages, b = j % kSBufs;
+                const int st = j % C::kStages, b = j % C::kSBufs;
                 ok = mbar_wait_bounded(bar_full(st), (j / C::kStages) & 1, abort_flag, kWaitLimit);
-                if (ok && j >= kSBufs)
-                    ok = mbar_wait_bounded(bar_sfree(b), ((j / kSBufs) - 1) & 1, abort_flag, kWaitLimit);
-                if (ok && *pv_issued < j - kSBufs + 1) {
+                if (ok && j >= C::kSBufs)
+                    ok = mbar_wait_bounded(bar_sfree(b), ((j / C::kSBufs) - 1) & 1, abort_flag, kWaitLimit);
+                if (ok && *pv_issued < j - C::kSBufs + 1) {
                     const long long t0 = clock64();
-                    while (*pv_issued < j - kSBufs + 1) {
+                    while (*pv_issued < j - C::kSBufs + 1) {
                         if (*abort_flag || clock64() - t0 > kWaitLimit) {
                             ok = false;
                             break;
@@ -484,25 +492,29 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                 if (!ok)
                     break;
                 tc_fence_after();
-                const uint32_t so = (uint32_t)(st * C::kStageBytes);
-                if constexpr (C::kStackQ) {
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        mma_f8_ss_warp(tmem_s0 + b * C::kSCols, adv(d_kv0, so + k * 32), adv(d_q0, k * 32), idesc_qk,
-                                       k > 0 ? 1u : 0u);
-                } else if constexpr (FP8) {
-#pragma unroll
-                    for (int t = 0; t < 2; ++t)
+                for (int hf = 0; hf < C::kHalves; ++hf) {
+                    // half hf: tokens [128 hf, 128 hf + 128) of the tile, 16 groups further on
+                    const uint32_t so = (uint32_t)(st * C::kStageBytes + hf * 16 * C::kGroupBytes);
+                    const uint32_t sd = tmem_s0 + b * C::kSBufCols + hf * C::kSCols;
+                    if constexpr (C::kStackQ) {
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
-                            mma_f8_ss_warp(tmem_s0 + b * RP, adv(d_kv0, so + k * 32), adv(d_q0, t * (RP * 128) + k * 32),
-                                           idesc_qk, (t > 0 || k > 0) ? 1u : 0u);
-                } else {
+                            mma_f8_ss_warp(sd, adv(d_kv0, so + k * 32), adv(d_q0, k * 32), idesc_qk, k > 0 ? 1u : 0u);
+                    } else if constexpr (FP8) {
 #pragma unroll
-                    for (int k = 0; k < kHeadDim / 16; ++k) {
-                        const uint32_t off = (uint32_t)((k >> 2) * 1024 + (k & 3) * 32);
-                        const uint32_t qoff = (uint32_t)((k >> 2) * (RP * 128) + (k & 3) * 32);
-                        mma_f16_ss_warp(tmem_s0 + b * RP, adv(d_kv0, so + off), adv(d_q0, qoff), idesc_qk, k > 0 ? 1u : 0u);
+                        for (int t = 0; t < 2; ++t)
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                mma_f8_ss_warp(sd, adv(d_kv0, so + k * 32), adv(d_q0, t * (RP * 128) + k * 32), idesc_qk,
+                                               (t > 0 || k > 0) ? 1u : 0u);
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < kHeadDim / 16; ++k) {
+                            const uint32_t off = (uint32_t)((k >> 2) * 1024 + (k & 3) * 32);
+                            const uint32_t qoff = (uint32_t)((k >> 2) * (RP * 128) + (k & 3) * 32);
+                            mma_f16_ss_warp(sd, adv(d_kv0, so + off), adv(d_q0, qoff), idesc_qk, k > 0 ? 1u : 0u);
+                        }
                     }
                 }
                 mma_commit_warp(bar_sfull(b));
@@ -514,13 +526,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                     atomicOr(p.status, SK_DEV_TIMEOUT);
                 }
                 if (last >= 0)     // let this warp's MMAs finish before TMEM is freed
-                    mbar_wait_bounded(bar_sfull(last % kSBufs), (last / kSBufs) & 1, nullptr, kWaitLimit);
+                    mbar_wait_bounded(bar_sfull(last % C::kSBufs), (last / C::kSBufs) & 1, nullptr, kWaitLimit);
             }
         } else {
             // PV(i) as soon as the softmax threads have written P(i).  Its completion frees the
             // stage (empty), which is also how the softmax learns that O holds tile i.
             for (int i = 0; i < ntiles && ok; ++i) {
-                ok = mbar_wait_bounded(bar_pfull(i % kSBufs), (i / kSBufs) & 1, abort_flag, kWaitLimit);
+                ok = mbar_wait_bounded(bar_pfull(i % C::kSBufs), (i / C::kSBufs) & 1, abort_flag, kWaitLimit);
                 ok = __all_sync(kFull, ok);
                 if (!ok)
                     break;
@@ -528,7 +540,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                 const uint32_t so = (uint32_t)((i % C::kStages) * C::kStageBytes);    // P^T over the dead K area
                 if constexpr (FP8) {
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
+                    for (int k = 0; k < C::kTile / 32; ++k)
                         mma_f8_ss_warp(tmem_o, adv(d_v0, so + k * 4 * C::kGroupBytes), adv(d_p0, so + k * 4 * C::kGroupBytes),
                                        idesc_pv, (i > 0 || k > 0) ? 1u : 0u);
                 } else {
@@ -581,26 +593,36 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
 
         for (int j = 0; j < ntiles; ++j) {
             const int b = j & 1;                // flags slot
-            const int sb = j % kSBufs;          // S buffer and its barriers
+            const int sb = j % C::kSBufs;          // S buffer and its barriers
             const int st = j % C::kStages;
-            float x[RH];
-            bool ok = !failed && mbar_wait_bounded(bar_sfull(sb), (j / kSBufs) & 1, abort_flag, kWaitLimit);
+            constexpr int NH = C::kHalves;
+            float x[NH][RH];                    // this thread's tokens: tau, 128 + tau
+            bool ok = !failed && mbar_wait_bounded(bar_sfull(sb), (j / C::kSBufs) & 1, abort_flag, kWaitLimit);
             ok = __all_sync(kFull, ok);          // tcgen05.ld is warp-collective
             if (ok) {
                 tc_fence_after();
-                const uint32_t s_col = tmem_s0 + sb * C::kSCols + r0 + lane_off;
 #pragma unroll
-                for (int c = 0; c < RH; c += kLd)
-                    tmem_ld32<kLd>(s_col + c, x + c);
-                if constexpr (C::kStackQ) {
-                    float y[RH];
+                for (int hf = 0; hf < NH; ++hf) {
+                    const uint32_t s_col = tmem_s0 + sb * C::kSBufCols + hf * C::kSCols + r0 + lane_off;
 #pragma unroll
                     for (int c = 0; c < RH; c += kLd)
-                        tmem_ld32<kLd>(s_col + RP + c, y + c);
+                        tmem_ld32<kLd>(s_col + c, x[hf] + c);
+                }
+                if constexpr (C::kStackQ) {
+                    float y[NH][RH];
+#pragma unroll
+                    for (int hf = 0; hf < NH; ++hf) {
+                        const uint32_t s_col = tmem_s0 + sb * C::kSBufCols + hf * C::kSCols + RP + r0 + lane_off;
+#pragma unroll
+                        for (int c = 0; c < RH; c += kLd)
+                            tmem_ld32<kLd>(s_col + c, y[hf] + c);
+                    }
                     tmem_wait_ld();
 #pragma unroll
-                    for (int r = 0; r < RH; ++r)
-                        x[r] += y[r];
+                    for (int hf = 0; hf < NH; ++hf)
+#pragma unroll
+                        for (int r = 0; r < RH; ++r)
+                            x[hf][r] += y[hf][r];
                 } else {
                     tmem_wait_ld();
                 }
@@ -609,31 +631,34 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(bar_sfree(sb));
-            // mask and scale: this thread's key is `tok`; row r = j' * G + i sees it when
-            // tok < segment end and (causal) j' >= tok - (L - q_len)
-            const int tok = k0 + j * kTokTile + tau;
-            const int ahead = tok - causal_base;       // > 0: only query tokens j' >= ahead see this key
-            const int rmin = ((p.causal && ahead > 0) ? ahead * p.G : 0) - row0;   // first local row that sees it
+            // mask and scale: this thread's key in half hf is `tok`; row r = j' * G + i sees it
+            // when tok < segment end and (causal) j' >= tok - (L - q_len)
             bool need = false;
-            // (padding rows r >= R have zero Q, so their scores are 0: harmless, and never written out)
-            if (ok && tok < k1 && rmin <= 0) {
 #pragma unroll
-                for (int r = 0; r < RH; r += 4) {
-                    const float4 t = *reinterpret_cast<const float4 *>(m_thr + r0 + r);
-                    const float4 c = *reinterpret_cast<const float4 *>(crow + r0 + r);
-                    x[r] *= c.x;
-                    x[r + 1] *= c.y;
-                    x[r + 2] *= c.z;
-                    x[r + 3] *= c.w;
-                    need |= (x[r] > t.x) | (x[r + 1] > t.y) | (x[r + 2] > t.z) | (x[r + 3] > t.w);
-                }
-            } else {
-                const bool tok_vis = ok && tok < k1;
+            for (int hf = 0; hf < NH; ++hf) {
+                const int tok = k0 + j * C::kTile + hf * kTokTile + tau;
+                const int ahead = tok - causal_base;       // > 0: only query tokens j' >= ahead see this key
+                const int rmin = ((p.causal && ahead > 0) ? ahead * p.G : 0) - row0;   // first local row that sees it
+                // (padding rows r >= R have zero Q, so their scores are 0: harmless, and never written out)
+                if (ok && tok < k1 && rmin <= 0) {
 #pragma unroll
-                for (int r = 0; r < RH; ++r) {
-                    const int rg = r0 + r;
-                    x[r] = (tok_vis && rg >= rmin && rg < R) ? x[r] * crow[rg] : -CUDART_INF_F;
-                    need |= x[r] > m_thr[rg];
+                    for (int r = 0; r < RH; r += 4) {
+                        const float4 t = *reinterpret_cast<const float4 *>(m_thr + r0 + r);
+                        const float4 c = *reinterpret_cast<const float4 *>(crow + r0 + r);
+                        x[hf][r] *= c.x;
+                        x[hf][r + 1] *= c.y;
+                        x[hf][r + 2] *= c.z;
+                        x[hf][r + 3] *= c.w;
+                        need |= (x[hf][r] > t.x) | (x[hf][r + 1] > t.y) | (x[hf][r + 2] > t.z) | (x[hf][r + 3] > t.w);
+                    }
+                } else {
+                    const bool tok_vis = ok && tok < k1;
+#pragma unroll
+                    for (int r = 0; r < RH; ++r) {
+                        const int rg = r0 + r;
+                        x[hf][r] = (tok_vis && rg >= rmin && rg < R) ? x[hf][r] * crow[rg] : -CUDART_INF_F;
+                        need |= x[hf][r] > m_thr[rg];
+                    }
                 }
             }
             // group decision: rescale needed? a wait failed?  (flags double-buffered by tile parity)
@@ -654,8 +679,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                 for (int c0 = 0; c0 < RH; c0 += kRc) {
                     float v[kRc];
 #pragma unroll
-                    for (int r = 0; r < kRc; ++r)
-                        v[r] = x[c0 + r];
+                    for (int r = 0; r < kRc; ++r) {
+                        v[r] = x[0][c0 + r];
+#pragma unroll
+                        for (int hf = 1; hf < NH; ++hf)
+                            v[r] = fmaxf(v[r], x[hf][c0 + r]);
+                    }
                     warp_transpose_reduce<kRc, true>(v, lane);
                     gred[tw * 32 + c0 + reduce_row0<kRc>(lane)] = v[0];
                 }
@@ -707,50 +736,55 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             if (!failed) {
                 // probabilities against the running max (masked entries are -inf -> 0), written as
                 // this token's row of P^T over the tile's K area, which QK(j) no longer needs:
-                // MN-major, 128-byte swizzle, 16-byte unit u of row tau stored at u ^ (tau % 8).
+                // MN-major, 128-byte swizzle, 16-byte unit u of row t stored at u ^ (t % 8).
                 // bf16: row r at bytes [2r, 2r + 2).  fp8: p * 2^kPShift = hi + lo, two e4m3 codes
                 // at bytes r and RP + r (the lo term is the f16 residual, which is exact).
-                uint8_t *prow = smem + st * C::kStageBytes + (tau >> 3) * C::kGroupBytes + (tau & 7) * 128;
 #pragma unroll
-                for (int u = 0; u < RH / 8; ++u) {
-                    const float4 ma = *reinterpret_cast<const float4 *>(m_sub + r0 + 8 * u);
-                    const float4 mb = *reinterpret_cast<const float4 *>(m_sub + r0 + 8 * u + 4);
-                    const float mm[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
-                    uint32_t pk[4];
+                for (int hf = 0; hf < NH; ++hf) {
+                    const int t = hf * kTokTile + tau;          // token of the tile
+                    uint8_t *prow = smem + st * C::kStageBytes + (t >> 3) * C::kGroupBytes + (t & 7) * 128;
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int r = 8 * u + 2 * e;
-                        const float p0 = ex2_ftz(x[r] - mm[2 * e]);
-                        const float p1 = ex2_ftz(x[r + 1] - mm[2 * e + 1]);
-                        lsum[r] += p0;
-                        lsum[r + 1] += p1;
-                        pk[e] = FP8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
-                    }
-                    if constexpr (FP8) {
-                        uint32_t hc[4], lc[4];
+                    for (int u = 0; u < RH / 8; ++u) {
+                        const float4 ma = *reinterpret_cast<const float4 *>(m_sub + r0 + 8 * u);
+                        const float4 mb = *reinterpret_cast<const float4 *>(m_sub + r0 + 8 * u + 4);
+                        const float mm[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
+                        uint32_t pk[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            hc[e] = f16x2_to_e4m3x2(pk[e]);
-                            lc[e] = f16x2_to_e4m3x2(sub_f16x2(pk[e], e4m3x2_to_f16x2(hc[e])));
+                            const int r = 8 * u + 2 * e;
+                            const float p0 = ex2_ftz(x[hf][r] - mm[2 * e]);
+                            const float p1 = ex2_ftz(x[hf][r + 1] - mm[2 * e + 1]);
+                            lsum[r] += p0;
+                            lsum[r + 1] += p1;
+                            pk[e] = FP8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
                         }
-                        const int bh = r0 + 8 * u, bl = RP + r0 + 8 * u;     // byte of the first row
-                        *reinterpret_cast<uint2 *>(prow + (((bh >> 4) ^ (tau & 7)) << 4) + (bh & 15)) =
-                            make_uint2(hc[0] | (hc[1] << 16), hc[2] | (hc[3] << 16));
-                        *reinterpret_cast<uint2 *>(prow + (((bl >> 4) ^ (tau & 7)) << 4) + (bl & 15)) =
-                            make_uint2(lc[0] | (lc[1] << 16), lc[2] | (lc[3] << 16));
-                    } else {
-                        const int ug = r0 / 8 + u;                 // unit of the row
-                        *reinterpret_cast<uint4 *>(prow + ((ug ^ (tau & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                    }
-                }
-                if (tok >= w.L && tok < last_page_end) {
-                    // past L in the last page the row holds anything (0 * NaN would reach O): this
-                    // group's half of the token's V row becomes zeros (bf16 chunk 2 + wg, fp8 64 bytes)
-                    uint8_t *vrow = smem + st * C::kStageBytes + C::kOffV + (tau >> 3) * C::kGroupBytes + (tau & 7) * 128 +
-                                    wg * (FP8 ? 64 : 1024);
+                        if constexpr (FP8) {
+                            uint32_t hc[4], lc[4];
 #pragma unroll
-                    for (int u = 0; u < (FP8 ? 4 : 8); ++u)
-                        *reinterpret_cast<uint4 *>(vrow + u * 16) = make_uint4(0u, 0u, 0u, 0u);
+                            for (int e = 0; e < 4; ++e) {
+                                hc[e] = f16x2_to_e4m3x2(pk[e]);
+                                lc[e] = f16x2_to_e4m3x2(sub_f16x2(pk[e], e4m3x2_to_f16x2(hc[e])));
+                            }
+                            const int bh = r0 + 8 * u, bl = RP + r0 + 8 * u;     // byte of the first row
+                            *reinterpret_cast<uint2 *>(prow + (((bh >> 4) ^ (t & 7)) << 4) + (bh & 15)) =
+                                make_uint2(hc[0] | (hc[1] << 16), hc[2] | (hc[3] << 16));
+                            *reinterpret_cast<uint2 *>(prow + (((bl >> 4) ^ (t & 7)) << 4) + (bl & 15)) =
+                                make_uint2(lc[0] | (lc[1] << 16), lc[2] | (lc[3] << 16));
+                        } else {
+                            const int ug = r0 / 8 + u;                 // unit of the row
+                            *reinterpret_cast<uint4 *>(prow + ((ug ^ (t & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        }
+                    }
+                    const int tok = k0 + j * C::kTile + t;
+                    if (tok >= w.L && tok < last_page_end) {
+                        // past L in the last page the row holds anything (0 * NaN would reach O): this
+                        // group's half of the token's V row becomes zeros (bf16 chunk 2 + wg, fp8 64 bytes)
+                        uint8_t *vrow = smem + st * C::kStageBytes + C::kOffV + (t >> 3) * C::kGroupBytes + (t & 7) * 128 +
+                                        wg * (FP8 ? 64 : 1024);
+#pragma unroll
+                        for (int u = 0; u < (FP8 ? 4 : 8); ++u)
+                            *reinterpret_cast<uint4 *>(vrow + u * 16) = make_uint4(0u, 0u, 0u, 0u);
+                    }
                 }
                 fence_proxy_async_smem();
             }
