@@ -60,7 +60,6 @@ namespace {
 using namespace sm100;
 
 constexpr int kTokTile = 128;                       // tokens per MMA (M)
-constexpr int kChunkRegion = kTokTile * 128;        // 16 KB: 128 token rows of 128 B
 constexpr int kSoftmaxWarp0 = 2;
 constexpr int kSoftmaxGroups = 2;                   // warpgroups splitting the query rows
 constexpr int kSoftmaxWarps = 4 * kSoftmaxGroups;
@@ -124,11 +123,10 @@ struct Cfg {
     static constexpr int kBarSFull = 16 * kStages;           // [kSBufs]
     static constexpr int kBarSFree = kBarSFull + 8 * kSBufs; // [kSBufs]
     static constexpr int kBarPFull = kBarSFree + 8 * kSBufs; // [kSBufs], by S buffer
-    static constexpr int kBarODone = kBarPFull + 8 * kSBufs; // committed once, after the last PV
+    static constexpr int kBarPvIs = kBarPFull + 8 * kSBufs;  // [kSBufs]: the PV of a tile issued
+    static constexpr int kBarODone = kBarPvIs + 8 * kSBufs;  // committed once, after the last PV
     static constexpr int kTmemSlot = kBarODone + 8;
     static constexpr int kAbort = kTmemSlot + 4;
-    static constexpr int kPvIssued = kAbort + 4;             // int: PVs issued so far (written by the PV thread)
-    static constexpr int kFlags = kPvIssued + 4;             // int[group][3][4]: per tile parity, then the epilogue
     static constexpr int kRed = 320;                         // float[group][4][32]
     static constexpr int kMrun = kRed + kSoftmaxGroups * 4 * 32 * 4;   // float[64] running max (log2 units)
     static constexpr int kMthr = kMrun + 64 * 4;             // float[64] running max + rescale threshold
@@ -136,7 +134,7 @@ struct Cfg {
     static constexpr int kAlpha = kMsub + 64 * 4;            // float[64]; reused for the final l
     static constexpr int kCrow = kAlpha + 64 * 4;            // float[64] per-row score scale (log2 units)
     static_assert(kStages >= 2, "shared memory");
-    static_assert(kFlags + kSoftmaxGroups * 48 <= kRed, "misc area");
+    static_assert(kAbort + 4 <= kRed, "misc area");
     static_assert(kCrow + 64 * 4 <= kMiscBytes, "misc area");
     static_assert(kSmemBytes <= kMaxSmem, "shared memory");
     static_assert(RP * kHeadDim * 4 <= kStageBytes * kStages, "epilogue staging");
@@ -202,13 +200,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return r;
 }
 
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
-{
-    uint32_t r;
-    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-
 // Two floats to packed e4m3 codes (lo in the low byte), nearest even, saturated to +-448.
 __device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi)
 {
@@ -223,21 +214,6 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v)
     uint32_t r;
     const uint16_t h = (uint16_t)(v & 0xFFFFu);
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(h));
-    return r;
-}
-
-// Packed f16 pair -> packed e4m3 pair (low 16 bits), nearest even, saturated to +-448.
-__device__ __forceinline__ uint32_t f16x2_to_e4m3x2(uint32_t v)
-{
-    uint16_t r;
-    asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(v));
-    return r;
-}
-
-__device__ __forceinline__ uint32_t sub_f16x2(uint32_t a, uint32_t b)
-{
-    uint32_t r;
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
     return r;
 }
 
@@ -287,7 +263,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
     uint8_t *misc = smem + C::kOffMisc;
     const uint32_t mbase = sbase + C::kOffMisc;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + C::kAbort);
-    volatile int *flags = reinterpret_cast<volatile int *>(misc + C::kFlags);
     float *red = reinterpret_cast<float *>(misc + C::kRed);
     float *m_run = reinterpret_cast<float *>(misc + C::kMrun);
     float *m_thr = reinterpret_cast<float *>(misc + C::kMthr);
@@ -299,7 +274,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
     auto bar_sfull = [&](int b) { return mbase + C::kBarSFull + 8 * b; };
     auto bar_sfree = [&](int b) { return mbase + C::kBarSFree + 8 * b; };
     auto bar_pfull = [&](int b) { return mbase + C::kBarPFull + 8 * b; };
-    volatile int *pv_issued = reinterpret_cast<volatile int *>(misc + C::kPvIssued);
+    auto bar_pvis = [&](int b) { return mbase + C::kBarPvIs + 8 * b; };
     const uint32_t bar_odone = mbase + C::kBarODone;
     const uint32_t q_s = sbase + C::kOffQ;
     auto stage = [&](int s) { return sbase + (uint32_t)(s * C::kStageBytes); };
@@ -317,10 +292,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             mbar_init(bar_sfull(b), 1);
             mbar_init(bar_sfree(b), kSoftmaxWarps);
             mbar_init(bar_pfull(b), kSoftmaxWarps);
+            mbar_init(bar_pvis(b), 1);
         }
         mbar_init(bar_odone, 1);
         *abort_flag = 0;
-        *pv_issued = 0;
         fence_mbar_init();
     }
     __syncthreads();   // barriers initialised: the producer starts its copies now
@@ -479,15 +454,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                 ok = mbar_wait_bounded(bar_full(st), (j / C::kStages) & 1, abort_flag, kWaitLimit);
                 if (ok && j >= C::kSBufs)
                     ok = mbar_wait_bounded(bar_sfree(b), ((j / C::kSBufs) - 1) & 1, abort_flag, kWaitLimit);
-                if (ok && *pv_issued < j - C::kSBufs + 1) {
-                    const long long t0 = clock64();
-                    while (*pv_issued < j - C::kSBufs + 1) {
-                        if (*abort_flag || clock64() - t0 > kWaitLimit) {
-                            ok = false;
-                            break;
-                        }
-                    }
-                }
+                if (ok && j >= C::kSBufs)     // PV(j - kSBufs) issued: phase j / kSBufs - 1 of pvis[b]
+                    ok = mbar_wait_bounded(bar_pvis(b), ((j / C::kSBufs) - 1) & 1, abort_flag, kWaitLimit);
                 ok = __all_sync(kFull, ok);
                 if (!ok)
                     break;
@@ -553,7 +521,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                 last = i;
                 __syncwarp();
                 if (lane == 0)
-                    *pv_issued = i + 1;
+                    mbar_arrive(bar_pvis(i % C::kSBufs));
             }
             if (last >= 0)
                 mma_commit_warp(bar_odone);   // completes once every PV issued has completed
@@ -584,7 +552,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
         const int causal_base = w.L - w.q_len;
         const int last_page_end = (w.L + kPage - 1) / kPage * kPage;
         bool failed = false;
-        volatile int *gflags = flags + wg * 12;
         float *gred = red + wg * (4 * 32);
         float lsum[RH];
 #pragma unroll
@@ -592,7 +559,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             lsum[r] = 0.f;
 
         for (int j = 0; j < ntiles; ++j) {
-            const int b = j & 1;                // flags slot
             const int sb = j % C::kSBufs;          // S buffer and its barriers
             const int st = j % C::kStages;
             constexpr int NH = C::kHalves;
@@ -661,18 +627,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                     }
                 }
             }
-            // group decision: rescale needed? a wait failed?  (flags double-buffered by tile parity)
-            const unsigned any_need = __any_sync(kFull, need);
-            const unsigned any_fail = __any_sync(kFull, !ok);
-            if (lane == 0)
-                gflags[4 * b + tw] = (any_need ? 1 : 0) | (any_fail ? 2 : 0);
-            named_bar_sync(bar_id, 128);
-            const int fl = gflags[4 * b] | gflags[4 * b + 1] | gflags[4 * b + 2] | gflags[4 * b + 3];
-            if (fl & 2) {
-                failed = true;
-                break;
-            }
-            if (fl & 1) {
+            // group decision, one reduction over the group's 128 threads: rescale needed or a wait
+            // failed?  Only then a second one tells which (every thread gets the same answers).
+            if (named_bar_or(bar_id, 128, need || !ok)) {
+                if (named_bar_or(bar_id, 128, !ok)) {
+                    failed = true;
+                    break;
+                }
                 // exact tile max of the group's rows across its 128 threads
                 constexpr int kRc = RH >= 32 ? 32 : RH;
 #pragma unroll
@@ -738,7 +699,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                 // this token's row of P^T over the tile's K area, which QK(j) no longer needs:
                 // MN-major, 128-byte swizzle, 16-byte unit u of row t stored at u ^ (t % 8).
                 // bf16: row r at bytes [2r, 2r + 2).  fp8: p * 2^kPShift = hi + lo, two e4m3 codes
-                // at bytes r and RP + r (the lo term is the f16 residual, which is exact).
+                // at bytes r and RP + r.
 #pragma unroll
                 for (int hf = 0; hf < NH; ++hf) {
                     const int t = hf * kTokTile + tau;          // token of the tile
@@ -748,7 +709,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                         const float4 ma = *reinterpret_cast<const float4 *>(m_sub + r0 + 8 * u);
                         const float4 mb = *reinterpret_cast<const float4 *>(m_sub + r0 + 8 * u + 4);
                         const float mm[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
-                        uint32_t pk[4];
+                        uint32_t pk[4], hc[4], lc[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const int r = 8 * u + 2 * e;
@@ -756,15 +717,19 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                             const float p1 = ex2_ftz(x[hf][r + 1] - mm[2 * e + 1]);
                             lsum[r] += p0;
                             lsum[r + 1] += p1;
-                            pk[e] = FP8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
+                            if constexpr (FP8) {
+                                // hi: p cut to 3 fraction bits (an e4m3 value when p >= 2^-6, else
+                                // rounded to the e4m3 subnormal grid, 2^-10 off at most); lo: the
+                                // exact f32 remainder, rounded to e4m3
+                                const float h0 = __uint_as_float(__float_as_uint(p0) & 0xFFF00000u);
+                                const float h1 = __uint_as_float(__float_as_uint(p1) & 0xFFF00000u);
+                                hc[e] = pack_e4m3x2(h0, h1);
+                                lc[e] = pack_e4m3x2(p0 - h0, p1 - h1);
+                            } else {
+                                pk[e] = pack_bf16x2(p0, p1);
+                            }
                         }
                         if constexpr (FP8) {
-                            uint32_t hc[4], lc[4];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                hc[e] = f16x2_to_e4m3x2(pk[e]);
-                                lc[e] = f16x2_to_e4m3x2(sub_f16x2(pk[e], e4m3x2_to_f16x2(hc[e])));
-                            }
                             const int bh = r0 + 8 * u, bl = RP + r0 + 8 * u;     // byte of the first row
                             *reinterpret_cast<uint2 *>(prow + (((bh >> 4) ^ (t & 7)) << 4) + (bh & 15)) =
                                 make_uint2(hc[0] | (hc[1] << 16), hc[2] | (hc[3] << 16));
@@ -803,14 +768,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
         bool okf = !failed;
         if (okf && ntiles > 0)
             okf = mbar_wait_bounded(bar_odone, 0, abort_flag, kWaitLimit);
-        okf = __all_sync(kFull, okf);
-        {
-            const unsigned any_fail = __any_sync(kFull, !okf);
-            if (lane == 0)
-                gflags[8 + tw] = any_fail ? 2 : 0;
-        }
-        named_bar_sync(bar_id, 128);
-        const bool write = ((gflags[8] | gflags[9] | gflags[10] | gflags[11]) & 2) == 0;
+        const bool write = !named_bar_or(bar_id, 128, !okf);
         {
             constexpr int kRc = RH >= 32 ? 32 : RH;
 #pragma unroll
