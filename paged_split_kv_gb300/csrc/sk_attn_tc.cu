@@ -704,6 +704,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                 for (int hf = 0; hf < NH; ++hf) {
                     const int t = hf * kTokTile + tau;          // token of the tile
                     uint8_t *prow = smem + st * C::kStageBytes + (t >> 3) * C::kGroupBytes + (t & 7) * 128;
+                    uint2 hprev = make_uint2(0u, 0u), lprev = make_uint2(0u, 0u);
 #pragma unroll
                     for (int u = 0; u < RH / 8; ++u) {
                         const float4 ma = *reinterpret_cast<const float4 *>(m_sub + r0 + 8 * u);
@@ -730,11 +731,26 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                             }
                         }
                         if constexpr (FP8) {
-                            const int bh = r0 + 8 * u, bl = RP + r0 + 8 * u;     // byte of the first row
-                            *reinterpret_cast<uint2 *>(prow + (((bh >> 4) ^ (t & 7)) << 4) + (bh & 15)) =
-                                make_uint2(hc[0] | (hc[1] << 16), hc[2] | (hc[3] << 16));
-                            *reinterpret_cast<uint2 *>(prow + (((bl >> 4) ^ (t & 7)) << 4) + (bl & 15)) =
-                                make_uint2(lc[0] | (lc[1] << 16), lc[2] | (lc[3] << 16));
+                            // 8 rows' hi and lo codes; with 16 rows per group they leave as two
+                            // 16-byte stores per 16 rows (one per term), else as 8-byte stores
+                            const uint2 h2 = make_uint2(hc[0] | (hc[1] << 16), hc[2] | (hc[3] << 16));
+                            const uint2 l2 = make_uint2(lc[0] | (lc[1] << 16), lc[2] | (lc[3] << 16));
+                            if constexpr (RH % 16 == 0) {
+                                if ((u & 1) == 0) {
+                                    hprev = h2;
+                                    lprev = l2;
+                                } else {
+                                    const int bh = r0 + 8 * (u - 1), bl = RP + bh;   // multiples of 16
+                                    *reinterpret_cast<uint4 *>(prow + (((bh >> 4) ^ (t & 7)) << 4)) =
+                                        make_uint4(hprev.x, hprev.y, h2.x, h2.y);
+                                    *reinterpret_cast<uint4 *>(prow + (((bl >> 4) ^ (t & 7)) << 4)) =
+                                        make_uint4(lprev.x, lprev.y, l2.x, l2.y);
+                                }
+                            } else {
+                                const int bh = r0 + 8 * u, bl = RP + r0 + 8 * u;     // byte of the first row
+                                *reinterpret_cast<uint2 *>(prow + (((bh >> 4) ^ (t & 7)) << 4) + (bh & 15)) = h2;
+                                *reinterpret_cast<uint2 *>(prow + (((bl >> 4) ^ (t & 7)) << 4) + (bl & 15)) = l2;
+                            }
                         } else {
                             const int ug = r0 / 8 + u;                 // unit of the row
                             *reinterpret_cast<uint4 *>(prow + ((ug ^ (t & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
