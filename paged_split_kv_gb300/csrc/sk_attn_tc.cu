@@ -283,6 +283,40 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
     const int ntiles = k1 > k0 ? (k1 - k0 + C::kTile - 1) / C::kTile : 0;
 
     // ---- set-up: barriers, TMEM, Q in shared memory (K-major, 128-byte swizzle)
+    // Q is read into registers before the producer starts, so that its loads are not queued
+    // behind every CTA's first copies.
+    constexpr uint32_t kSetupBar = 3;
+    constexpr int kSetupThreads = kThreads - 32;
+    const int st_tid = threadIdx.x - 32;
+    constexpr int kQUnits = FP8 ? (RP + kSetupThreads / 32 - 1) / (kSetupThreads / 32)   // rows per warp
+                                : (RP * 16 + kSetupThreads - 1) / kSetupThreads;         // 16-byte units per thread
+    uint4 qpre[FP8 ? 1 : kQUnits];
+    uint2 qraw[FP8 ? kQUnits : 1];
+    if (warp != 0) {
+        if constexpr (!FP8) {
+#pragma unroll
+            for (int k = 0; k < kQUnits; ++k) {
+                const int u = st_tid + k * kSetupThreads, r = u >> 4, unit = u & 15;
+                qpre[k] = make_uint4(0u, 0u, 0u, 0u);
+                if (u < RP * 16 && r < R) {
+                    const int j = (row0 + r) / p.G, i = row0 + r - j * p.G;
+                    const uint16_t *src = p.q + ((long long)(w.tok0 + j) * p.H_q + h * p.G + i) * kHeadDim + unit * 8;
+                    qpre[k] = __ldg(reinterpret_cast<const uint4 *>(src));
+                }
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < kQUnits; ++k) {
+                const int r = warp - 1 + k * (kSetupThreads / 32);
+                qraw[k] = make_uint2(0u, 0u);
+                if (r < R) {
+                    const int j = (row0 + r) / p.G, i = row0 + r - j * p.G;
+                    qraw[k] = __ldg(reinterpret_cast<const uint2 *>(
+                        p.q + ((long long)(w.tok0 + j) * p.H_q + h * p.G + i) * kHeadDim + lane * 4));
+                }
+            }
+        }
+    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(bar_full(s), 1);
@@ -300,42 +334,36 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
     }
     __syncthreads();   // barriers initialised: the producer starts its copies now
     // The other warps set up TMEM and Q meanwhile, then meet at a barrier of their own.
-    constexpr uint32_t kSetupBar = 3;
-    constexpr int kSetupThreads = kThreads - 32;
-    const int st_tid = threadIdx.x - 32;
     if (warp != 0) {
         if (warp == 1) {
             tmem_alloc(mbase + C::kTmemSlot, C::kTmemCols);
             tmem_relinquish();
         }
         if constexpr (!FP8) {
-            for (int u = st_tid; u < RP * 16; u += kSetupThreads) {
-                const int r = u >> 4, unit = u & 15;
-                uint4 val = make_uint4(0u, 0u, 0u, 0u);
-                if (r < R) {
-                    const int j = (row0 + r) / p.G, i = row0 + r - j * p.G;
-                    const uint16_t *src = p.q + ((long long)(w.tok0 + j) * p.H_q + h * p.G + i) * kHeadDim + unit * 8;
-                    val = __ldg(reinterpret_cast<const uint4 *>(src));
-                }
+#pragma unroll
+            for (int k = 0; k < kQUnits; ++k) {
+                const int u = st_tid + k * kSetupThreads, r = u >> 4, unit = u & 15;
                 const int chunk = unit >> 3, uu = unit & 7;
-                st_shared_v4(q_s + chunk * (RP * 128) + r * 128 + ((uu ^ (r & 7)) << 4), val.x, val.y, val.z, val.w);
+                if (u < RP * 16)
+                    st_shared_v4(q_s + chunk * (RP * 128) + r * 128 + ((uu ^ (r & 7)) << 4), qpre[k].x, qpre[k].y,
+                                 qpre[k].z, qpre[k].w);
             }
             for (int r = st_tid; r < RP; r += kSetupThreads)
                 crow[r] = p.score_scale_log2;
         } else {
             // Row r of Q scaled by 2^e (max |q| lands in [128, 256)), as two e4m3 terms hi + lo.
             // One warp per row; lane l owns dimensions 4l..4l+3.
-            for (int r = warp - 1; r < RP; r += kSetupThreads / 32) {
-                float qv[4] = {0.f, 0.f, 0.f, 0.f};
-                if (r < R) {
-                    const int j = (row0 + r) / p.G, i = row0 + r - j * p.G;
-                    const uint2 raw = __ldg(reinterpret_cast<const uint2 *>(
-                        p.q + ((long long)(w.tok0 + j) * p.H_q + h * p.G + i) * kHeadDim + lane * 4));
-                    qv[0] = __uint_as_float(raw.x << 16);
-                    qv[1] = __uint_as_float(raw.x & 0xFFFF0000u);
-                    qv[2] = __uint_as_float(raw.y << 16);
-                    qv[3] = __uint_as_float(raw.y & 0xFFFF0000u);
-                }
+#pragma unroll
+            for (int k = 0; k < kQUnits; ++k) {
+                const int r = warp - 1 + k * (kSetupThreads / 32);
+                if (r >= RP)
+                    break;
+                const uint2 raw = qraw[k];                   // zeros past the item's rows
+                float qv[4];
+                qv[0] = __uint_as_float(raw.x << 16);
+                qv[1] = __uint_as_float(raw.x & 0xFFFF0000u);
+                qv[2] = __uint_as_float(raw.y << 16);
+                qv[3] = __uint_as_float(raw.y & 0xFFFF0000u);
                 float amax = fmaxf(fmaxf(fabsf(qv[0]), fabsf(qv[1])), fmaxf(fabsf(qv[2]), fabsf(qv[3])));
                 for (int o = 16; o > 0; o >>= 1)
                     amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
@@ -386,9 +414,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
         const int page0 = k0 / kPage;
         const int page_end = (k1 + kPage - 1) / kPage;
         const int32_t *bt_row = p.block_table + (long long)w.s * p.bt_stride;
-        int blk_next = -1;
-        if (lane < C::kPagesPerTile && page0 + lane < page_end)
-            blk_next = __ldg(bt_row + page0 + lane);
+        // block ids of the next kStages tiles (one page per lane), fetched a full ring ahead:
+        // q_blk[s] belongs to tile j + s, so the first copies go out back to back
+        int q_blk[C::kStages];
+#pragma unroll
+        for (int s2 = 0; s2 < C::kStages; ++s2) {
+            const int pg = page0 + s2 * C::kPagesPerTile + lane;
+            q_blk[s2] = (lane < C::kPagesPerTile && s2 < ntiles && pg < page_end) ? __ldg(bt_row + pg) : -1;
+        }
         int issued = 0;
         bool ok = true;
         for (int j = 0; j < ntiles && ok; ++j) {
@@ -398,12 +431,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             ok = __all_sync(kFull, ok);
             if (!ok)
                 break;
-            const int blk = blk_next;
+            const int blk = q_blk[0];
             const int pg = page0 + j * C::kPagesPerTile + lane;
-            const int pg_next = pg + C::kPagesPerTile;
-            blk_next = -1;
-            if (lane < C::kPagesPerTile && j + 1 < ntiles && pg_next < page_end)
-                blk_next = __ldg(bt_row + pg_next);
+            const int pg_far = pg + C::kStages * C::kPagesPerTile;     // tile j + kStages
+#pragma unroll
+            for (int s2 = 0; s2 + 1 < C::kStages; ++s2)
+                q_blk[s2] = q_blk[s2 + 1];
+            q_blk[C::kStages - 1] = (lane < C::kPagesPerTile && j + C::kStages < ntiles && pg_far < page_end)
+                                        ? __ldg(bt_row + pg_far) : -1;
             if (lane == 0)
                 mbar_arrive_expect_tx(bar_full(st), C::kTxBytes);
             __syncwarp();
