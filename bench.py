@@ -372,9 +372,10 @@ def run_sk(a, w, ws, rank, local):
     flush_rd = None if flush is None else torch.ones(256 << 20, dtype=torch.uint8, device=dev)
     flush_sink = None if flush is None else torch.zeros(1, dtype=torch.int64, device=dev)
     # The timed steps are captured once as a CUDA graph (every call is capture safe), with an
-    # event pair around each kernel recorded inside the graph, and replayed once: the device
-    # runs exactly the kernels of K eager steps, but the timing does not depend on how fast
-    # the host can issue ~15 calls a step.  --eager keeps the Python-launched loop.
+    # event pair around each step recorded inside the graph, and replayed once: the device runs
+    # exactly the kernels of K eager steps, but the timing does not depend on how fast the host
+    # can issue the calls.  A second graph of the same steps, with events around each kernel,
+    # gives the per-kernel split.  --eager keeps the Python-launched loops.
     try:
         graph_events = not a.eager and torch.cuda.Event(enable_timing=True, external=True) is not None
     except TypeError:                      # a PyTorch without graph-recorded events
@@ -382,6 +383,10 @@ def run_sk(a, w, ws, rank, local):
     stream = torch.cuda.Stream(device=dev) if graph_events else torch.cuda.current_stream()
 
     def step(ev=None):
+        # ev: None, [start, end] of the step, or [start, after plan, after attention, end].  Events
+        # between kernels cut the launch overlap of dependent kernels, so the timed steps carry the
+        # pair only and a second replay of the same steps gives the per-kernel split.
+        parts = ev is not None and len(ev) == 4
         if flush is not None:
             flush.fill_(1)
             torch.sum(flush_rd.view(torch.int64), dim=0, keepdim=True, out=flush_sink)
@@ -390,17 +395,17 @@ def run_sk(a, w, ws, rank, local):
         if use_plan:
             sk.sk_plan_cache_reset()
             sk.sk_build_plan(lens, cu, hkv, plan, tok, nsm, w.seg_max, stream)
-        if ev is not None:
+        if parts:
             ev[1].record(stream)
         sk.sk_paged_decode_attn(q, kv, bt, lens, cu, plan, part_o, part_m, part_l,
                                 max_q_len=w.max_q_len, sm_scale=w.sm_scale, num_sms=nsm,
                                 k_scale=w.k_scale, v_scale=w.v_scale, causal=bool(w.causal),
                                 stream=stream)
-        if ev is not None:
+        if parts:
             ev[2].record(stream)
         sk.sk_merge_segments(part_o, part_m, part_l, tok, out, lse, fixed_nseg=fixed, stream=stream)
         if ev is not None:
-            ev[3].record(stream)
+            ev[-1].record(stream)
 
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
@@ -411,8 +416,9 @@ def run_sk(a, w, ws, rank, local):
             step()
     torch.cuda.synchronize()
     if graph_events:
-        evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)] for _ in range(a.steps)]
-        g_warm, g_timed = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)] for _ in range(a.steps)]
+        evp = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)] for _ in range(a.steps)]
+        g_warm, g_timed, g_parts = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
             with torch.cuda.graph(g_warm, stream=stream):
                 for _ in range(max(3, a.warmup)):
@@ -420,9 +426,13 @@ def run_sk(a, w, ws, rank, local):
             with torch.cuda.graph(g_timed, stream=stream):
                 for i in range(a.steps):
                     step(evs[i])
+            with torch.cuda.graph(g_parts, stream=stream):
+                for i in range(a.steps):
+                    step(evp[i])
         g_warm.replay()
     else:
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(a.steps)]
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(a.steps)]
+        evp = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(a.steps)]
         for _ in range(max(3, a.warmup)):
             step()
     torch.cuda.synchronize()
@@ -439,15 +449,22 @@ def run_sk(a, w, ws, rank, local):
         for i in range(a.steps):
             step(evs[i])
     torch.cuda.synchronize()
-    clocks = sampler.stop() if sampler else None
     if ws > 1:
         torch.distributed.barrier()
-    plan_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    attn_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    merge_ms = [e[2].elapsed_time(e[3]) for e in evs]
-    # with a flush, the timed region is the steps themselves (each ev[0] -> ev[3]), flushes excluded
-    local_ms = (sum(e[0].elapsed_time(e[3]) for e in evs) if flush is not None
-                else evs[0][0].elapsed_time(evs[-1][3]))
+    # the per-kernel split: the same steps again, with an event pair around each kernel
+    if graph_events:
+        g_parts.replay()
+    else:
+        for i in range(a.steps):
+            step(evp[i])
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    plan_ms = [e[0].elapsed_time(e[1]) for e in evp]
+    attn_ms = [e[1].elapsed_time(e[2]) for e in evp]
+    merge_ms = [e[2].elapsed_time(e[3]) for e in evp]
+    # with a flush, the timed region is the steps themselves (each ev[0] -> ev[1]), flushes excluded
+    local_ms = (sum(e[0].elapsed_time(e[1]) for e in evs) if flush is not None
+                else evs[0][0].elapsed_time(evs[-1][1]))
     total_ms = max_over_ranks(local_ms, ws, dev)
     ms_per_step = total_ms / a.steps
     value = weak_scaling_tbps(w.kv_bytes, a.steps, ws, total_ms)
@@ -551,7 +568,9 @@ def run_sk(a, w, ws, rank, local):
             "frac_of_8tbps_nominal": round(value / 8.0, 4),
             "roofline": roofline, "clocks": clocks, "e2e": e2e, "e2e_serving": e2e_serving, "cpu_baseline": cpu,
             "gpu_launches": a.steps * (3 if use_plan else 2),
-            "launch": "timed steps replayed as one CUDA graph" if graph_events else "eager, one Python call per kernel"}
+            "launch": ("timed steps replayed as one CUDA graph (events around each step; the per-kernel split "
+                       "comes from a second replay with events around each kernel)") if graph_events
+                      else "eager, one Python call per kernel"}
     print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()

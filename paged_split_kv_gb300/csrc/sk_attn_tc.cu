@@ -238,6 +238,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
     using C = Cfg<RP, FP8>;
     extern __shared__ __align__(1024) uint8_t smem[];
 
+    wait_prior_grid();    // the plan, Q and the pages may come from the kernels before this one
     // CTA b: row block b % row_blocks (neighbouring CTAs share a work item's pages, so
     // the later reads of a page find it in L2) of work item / KV head b / row_blocks.
     const int ih = blockIdx.x / p.row_blocks;
@@ -814,12 +815,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             }
         }
 
-        // ---- epilogue: O complete?  then row sums across the group's threads and the partials
-        // (a stage barrier cannot tell PV(last) from PV(last-1) here: both may still be running)
-        bool okf = !failed;
-        if (okf && ntiles > 0)
-            okf = mbar_wait_bounded(bar_odone, 0, abort_flag, kWaitLimit);
-        const bool write = !named_bar_or(bar_id, 128, !okf);
+        // ---- epilogue: row sums across the group's threads (they do not need the last PV, which
+        // completes meanwhile), then O complete? and the partials.  (A stage barrier cannot tell
+        // PV(last) from PV(last-1) here: both may still be running; bar_odone can.)
         {
             constexpr int kRc = RH >= 32 ? 32 : RH;
 #pragma unroll
@@ -835,7 +833,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
         named_bar_sync(bar_id, 128);
         if (tid < RH)
             alpha_s[r0 + tid] = (gred[tid] + gred[32 + tid]) + (gred[64 + tid] + gred[96 + tid]);
-        named_bar_sync(bar_id, 128);
+        bool okf = !failed;
+        if (okf && ntiles > 0)
+            okf = mbar_wait_bounded(bar_odone, 0, abort_flag, kWaitLimit);
+        // the group's verdict; the barrier also publishes the row sums written above
+        const bool write = !named_bar_or(bar_id, 128, !okf);
         if (write) {
             // O^T of the group's rows -> stage 0 as [row][128] fp32 (every copy and MMA is done:
             // the stages are free), then one 512-byte bulk store per row into the partials
@@ -924,8 +926,7 @@ cudaError_t launch_rp(const CUtensorMap &map, const AttnParams &p, cudaStream_t 
     if (attr_err != cudaSuccess)
         return attr_err;
     const dim3 grid((unsigned)p.num_items * (unsigned)p.H_kv * (unsigned)p.row_blocks);
-    attn_tc_kernel<RP, FP8><<<grid, kThreads, Cfg<RP, FP8>::kSmemBytes, stream>>>(map, p);
-    return cudaGetLastError();
+    return launch_pdl(attn_tc_kernel<RP, FP8>, grid, dim3(kThreads), Cfg<RP, FP8>::kSmemBytes, stream, map, p);
 }
 
 }  // namespace

@@ -97,6 +97,34 @@ __device__ __forceinline__ int visible_keys(int L, int q_len, int j, int causal)
     return n > 0 ? n : 0;
 }
 
+// Programmatic dependent launch.  Every kernel of the library is launched with
+// launch_pdl, so it may begin while the kernel before it on the stream is still
+// finishing (its launch latency then overlaps that kernel's tail).  Each kernel
+// calls wait_prior_grid() before it reads anything an earlier kernel may have
+// written; the call waits until that kernel has completed and its writes are
+// visible, and returns at once when there is no such kernel.
+__device__ __forceinline__ void wait_prior_grid()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Address of the current device's status word (looked up once per device).
 int device_status_word(int **out);
 // Records `msg` as this thread's last error and returns `code`.

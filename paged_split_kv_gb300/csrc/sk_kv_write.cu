@@ -59,6 +59,7 @@ kv_write_kernel(const uint16_t *__restrict__ key, const uint16_t *__restrict__ v
                 const int64_t *__restrict__ slot_mapping, long long rows, int H, long long num_slots,
                 void *__restrict__ pages, float k_scale, float v_scale, int *status)
 {
+    wait_prior_grid();    // K, V and the slots may come from the kernels before this one
     const int lane = threadIdx.x & 31;
     const long long warp0 = (long long)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
     const long long nwarps = (long long)gridDim.x * (kThreads / 32);
@@ -126,16 +127,11 @@ cudaError_t launch_kv_write(const uint16_t *key, const uint16_t *value, const in
         return m == 0.5f && r * sc == 1.f && std::isnormal(r) && std::isnormal(sc);
     };
     const dim3 grid((unsigned)blocks);
-    if (kv_dtype != SK_KV_FP8_E4M3)
-        kv_write_kernel<false, false><<<grid, kThreads, 0, stream>>>(key, value, slot_mapping, rows, num_kv_heads,
-                                                                     num_slots, pages, k_scale, v_scale, status);
-    else if (exact_recip(k_scale) && exact_recip(v_scale))
-        kv_write_kernel<true, true><<<grid, kThreads, 0, stream>>>(key, value, slot_mapping, rows, num_kv_heads,
-                                                                   num_slots, pages, k_scale, v_scale, status);
-    else
-        kv_write_kernel<true, false><<<grid, kThreads, 0, stream>>>(key, value, slot_mapping, rows, num_kv_heads,
-                                                                    num_slots, pages, k_scale, v_scale, status);
-    return cudaGetLastError();
+    auto kernel = kv_dtype != SK_KV_FP8_E4M3                     ? kv_write_kernel<false, false>
+                  : (exact_recip(k_scale) && exact_recip(v_scale)) ? kv_write_kernel<true, true>
+                                                                   : kv_write_kernel<true, false>;
+    return launch_pdl(kernel, grid, dim3(kThreads), 0, stream, key, value, slot_mapping, rows, num_kv_heads, num_slots,
+                      pages, k_scale, v_scale, status);
 }
 
 }  // namespace sk

@@ -44,6 +44,7 @@ merge_kernel(const float *__restrict__ part_o, const float *__restrict__ part_m,
 {
     constexpr int kRowsPerCta = (kThreads / 32) / WPR;
     __shared__ float4 acc_s[kThreads / 32][32];
+    wait_prior_grid();    // the partials come from the attention kernel
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int sub = warp % WPR;                       // this warp's share of the row's segments
     const long long row = (long long)blockIdx.x * kRowsPerCta + warp / WPR;
@@ -169,16 +170,15 @@ cudaError_t launch_merge(const float *part_o, const float *part_m, const float *
     if (tok_nseg == nullptr && fixed_nseg >= 16) {
         if (rows > 0x7FFFFFFFLL)
             return cudaErrorInvalidValue;
-        merge_kernel<4><<<(unsigned)rows, kThreads, 0, stream>>>(part_o, part_m, part_l, tok_nseg, fixed_nseg,
-                                                                rows, H_q, seg_max, out, lse);
+        return launch_pdl(merge_kernel<4>, dim3((unsigned)rows), dim3(kThreads), 0, stream, part_o, part_m, part_l,
+                          tok_nseg, fixed_nseg, rows, H_q, seg_max, out, lse);
     } else {
         const long long grid = (rows + kThreads / 32 - 1) / (kThreads / 32);
         if (grid > 0x7FFFFFFFLL)
             return cudaErrorInvalidValue;
-        merge_kernel<1><<<(unsigned)grid, kThreads, 0, stream>>>(part_o, part_m, part_l, tok_nseg, fixed_nseg,
-                                                                 rows, H_q, seg_max, out, lse);
+        return launch_pdl(merge_kernel<1>, dim3((unsigned)grid), dim3(kThreads), 0, stream, part_o, part_m, part_l,
+                          tok_nseg, fixed_nseg, rows, H_q, seg_max, out, lse);
     }
-    return cudaGetLastError();
 }
 
 }  // namespace sk

@@ -66,6 +66,7 @@ plan_kernel(const int32_t *__restrict__ seq_lens, const int32_t *__restrict__ cu
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nthr = blockDim.x, nwarps = nthr >> 5;
     const bool cached = bs <= kCacheSeqs;
+    wait_prior_grid();    // the lengths may come from a kernel before this one
     // tile counts are below 2^26 (lengths are int32), so they and T fit in 32 bits
     auto tiles_at = [&](int s) -> uint32_t {
         return cached ? (uint32_t)tiles_s[s] : (uint32_t)tiles_of(__ldg(seq_lens + s));
@@ -210,9 +211,8 @@ cudaError_t launch_plan(const int32_t *seq_lens, const int32_t *cu_q, int bs, in
 {
     const int warps = (bs + 31) / 32;
     const int threads = 32 * (warps < 1 ? 1 : warps > kPlanMaxThreads / 32 ? kPlanMaxThreads / 32 : warps);
-    plan_kernel<<<1, threads, 0, stream>>>(seq_lens, cu_q, bs, num_tokens, budget, seg_max, plan,
-                                           plan_capacity, tok_nseg, status);
-    return cudaGetLastError();
+    return launch_pdl(plan_kernel, dim3(1), dim3(threads), 0, stream, seq_lens, cu_q, bs, num_tokens, budget,
+                      seg_max, plan, plan_capacity, tok_nseg, status);
 }
 
 }  // namespace sk

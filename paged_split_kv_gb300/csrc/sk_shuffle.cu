@@ -56,6 +56,7 @@ std_to_shuffled_kernel(const uint8_t *__restrict__ pages, const int32_t *__restr
     constexpr int kUnitsPerRow = kRowBytes / 16;
     constexpr int kKUnits = kHeadBytes / 32;            // 16-byte units of K (half the page)
     __shared__ __align__(16) uint8_t buf[kWarps][kPage * kRowS];
+    wait_prior_grid();    // the pages may come from the kernels before this one
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint8_t *sb = buf[warp];
     for (long long u = (long long)blockIdx.x * kWarps + warp; u < num_units; u += (long long)gridDim.x * kWarps) {
@@ -143,13 +144,9 @@ cudaError_t launch_std_to_shuffled(const void *pages, int kv_dtype, const int32_
     const auto *src = static_cast<const uint8_t *>(pages);
     auto *ko = static_cast<uint8_t *>(k_out);
     auto *vo = static_cast<uint8_t *>(v_out);
-    if (kv_dtype == SK_KV_FP8_E4M3)
-        std_to_shuffled_kernel<true><<<(unsigned)blocks, 32 * kWarps, 0, stream>>>(src, ids, units, num_kv_heads,
-                                                                                   num_blocks, ko, vo, status);
-    else
-        std_to_shuffled_kernel<false><<<(unsigned)blocks, 32 * kWarps, 0, stream>>>(src, ids, units, num_kv_heads,
-                                                                                    num_blocks, ko, vo, status);
-    return cudaGetLastError();
+    auto kernel = kv_dtype == SK_KV_FP8_E4M3 ? std_to_shuffled_kernel<true> : std_to_shuffled_kernel<false>;
+    return launch_pdl(kernel, dim3((unsigned)blocks), dim3(32 * kWarps), 0, stream, src, ids, units, num_kv_heads,
+                      num_blocks, ko, vo, status);
 }
 
 }  // namespace sk
