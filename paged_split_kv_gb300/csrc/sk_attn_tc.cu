@@ -318,6 +318,19 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             }
         }
     }
+    // The producer's block ids for the first kStages tiles (one page per lane), read before the
+    // barriers are set up; later it keeps them a full ring of tiles ahead: q_blk[s] belongs to
+    // tile j + s, so the first copies go out back to back.
+    int q_blk[C::kStages];
+    if (warp == 0) {
+        const int pg0 = k0 / kPage, pge = (k1 + kPage - 1) / kPage;
+        const int32_t *btr = p.block_table + (long long)w.s * p.bt_stride;
+#pragma unroll
+        for (int s2 = 0; s2 < C::kStages; ++s2) {
+            const int pg = pg0 + s2 * C::kPagesPerTile + lane;
+            q_blk[s2] = (lane < C::kPagesPerTile && s2 < ntiles && pg < pge) ? __ldg(btr + pg) : -1;
+        }
+    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(bar_full(s), 1);
@@ -415,14 +428,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
         const int page0 = k0 / kPage;
         const int page_end = (k1 + kPage - 1) / kPage;
         const int32_t *bt_row = p.block_table + (long long)w.s * p.bt_stride;
-        // block ids of the next kStages tiles (one page per lane), fetched a full ring ahead:
-        // q_blk[s] belongs to tile j + s, so the first copies go out back to back
-        int q_blk[C::kStages];
-#pragma unroll
-        for (int s2 = 0; s2 < C::kStages; ++s2) {
-            const int pg = page0 + s2 * C::kPagesPerTile + lane;
-            q_blk[s2] = (lane < C::kPagesPerTile && s2 < ntiles && pg < page_end) ? __ldg(bt_row + pg) : -1;
-        }
         int issued = 0;
         bool ok = true;
         for (int j = 0; j < ntiles && ok; ++j) {
