@@ -2,38 +2,43 @@
 //
 // One CTA per (sequence, segment, KV head) work item, as in SGLang PR 39172
 // (Modifications, second item).  The GQA group's R = G * q_len query rows
-// share every K/V byte, so the two products of a 128-token tile are dense
-// contractions:
-//     S^T [128 tokens x R] = K_tile [128 x 128 dims] . Q^T
-//     O^T [128 dims   x R] += V_tile^T [128 dims x 128 tokens] . P^T
+// share every K/V byte, so the two products of a tile are dense contractions
+// (per 128 tokens):
+//     S^T [128 tokens x R] = K_half [128 x 128 dims] . Q^T
+//     O^T [128 dims   x R] += V_tile^T [128 dims x tile tokens] . P^T
 // Tokens and dimensions take the MMA's M = 128 and the query rows its N
-// (16, 32 or 64 columns).  S^T (four buffers) and O^T live in tensor memory
-// (TMEM lane = token for S, = dimension for O).  An item with more than 64
+// (16, 32 or 64 columns).  S^T (four buffers of a 128-token tile, or two of a
+// 256-token one) and O^T live in tensor memory (TMEM lane = token for S, =
+// dimension for O).  An item with more than 64
 // rows is split into row blocks of 64, one CTA each, placed next to each other
 // so that they stream the same pages at about the same time (L2 serves the
 // repeats).
 //
 // Roles (352 threads):
-//   warp 0   TMA producer: one 4-D copy per page (8 per 128-token tile) into
+//   warp 0   TMA producer: one 4-D copy per page (8 or 16 per tile) into
 //            128-byte-swizzled atoms that are at once the K-major K operand
 //            and the MN-major V^T operand (layout below).  Pages past the
 //            segment end are out-of-bounds boxes: zero-filled, no HBM traffic.
-//            It starts as soon as the mbarriers exist.
+//            It starts as soon as the mbarriers exist, with the block ids of
+//            its first tiles already read; later it reads them a ring ahead.
 //   warp 1   allocates TMEM; issues the QK products.
 //   warp 10  issues the PV products.  Both issuers run converged and issue
 //            through one elected lane, so the descriptors stay warp-uniform.
-//   warps 2-9  softmax, two warpgroups: one thread per token of the tile (its
-//            TMEM lane); warps 2-5 take the first half of the query rows,
-//            warps 6-9 the second, each group on its own.
+//   warps 2-9  softmax, two warpgroups: one thread per token of each 128-token
+//            half of the tile (its TMEM lane); warps 2-5 take the first half of
+//            the query rows, warps 6-9 the second, each group on its own.
 //            The running max per query row is kept lazily: scores are
 //            exponentiated against the current max unless one beats it by
-//            2^8, and only then is the tile max reduced across the 128
-//            threads and O rescaled (which waits for the previous PV).
+//            2^8 (2^4 for fp8), which the group decides with one bar.red per
+//            tile; only then is the tile max reduced across the 128 threads
+//            and O rescaled (which waits for the previous PV).
 //            Row sums are kept per thread and reduced once at the end.
 //            P^T is written over the tile's own K area, which QK no longer
 //            needs, so every stage carries its own P buffer.
 // fp8 pages: both products run as kind::f8f6f4 on the e4m3 codes as they
-// arrive, so a stage is only the tile's 32 KB of codes and six stages fit.
+// arrive, so a stage holds only codes: a 256-token tile (64 KB, three stages)
+// for up to 32 rows, whose single softmax pass covers as many bytes as a bf16
+// tile's, else a 128-token tile (32 KB, six stages).
 // QK splits Q into two e4m3 terms (q * 2^e_r = hi + lo, a power-of-two scale
 // per row): for up to 32 rows the two terms are one stacked operand (S_hi |
 // S_lo, added by the softmax), else two products into the same S.  PV splits
