@@ -138,11 +138,11 @@ struct Cfg {
     static constexpr int kMsub = kMthr + 64 * 4;             // float[64] running max - kPShift, -inf -> 0
     static constexpr int kAlpha = kMsub + 64 * 4;            // float[64]; reused for the final l
     static constexpr int kCrow = kAlpha + 64 * 4;            // float[64] per-row score scale (log2 units)
+    static constexpr int kSlot = kCrow + 64 * 4;             // long long[64]: partial slot of each row
     static_assert(kStages >= 2, "shared memory");
     static_assert(kAbort + 4 <= kRed, "misc area");
-    static_assert(kCrow + 64 * 4 <= kMiscBytes, "misc area");
+    static_assert(kSlot + 64 * 8 <= kMiscBytes, "misc area");
     static_assert(kSmemBytes <= kMaxSmem, "shared memory");
-    static_assert(RP * kHeadDim * 4 <= kStageBytes * kStages, "epilogue staging");
     static_assert((kOffQ % 1024) == 0 && (kMrun % 16) == 0 && (kMthr % 16) == 0 && (kMsub % 16) == 0 &&
                       (kCrow % 16) == 0,
                   "operand and vector alignment");
@@ -414,6 +414,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             }
         }
         for (int r = st_tid; r < RP; r += kSetupThreads) {
+            long long slot = -1;
+            if (r < R) {
+                const int jq = (row0 + r) / p.G, i = row0 + r - jq * p.G;
+                slot = (long long)(w.tok0 + jq) * p.seg_max * p.H_q + (long long)w.g * p.H_q + h * p.G + i;
+            }
+            reinterpret_cast<long long *>(misc + C::kSlot)[r] = slot;
             m_run[r] = -CUDART_INF_F;
             m_thr[r] = -CUDART_INF_F;
             m_sub[r] = 0.f;
@@ -858,11 +864,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
         // the group's verdict; the barrier also publishes the row sums written above
         const bool write = !named_bar_or(bar_id, 128, !okf);
         if (write) {
-            // O^T of the group's rows -> stage 0 as [row][128] fp32 (every copy and MMA is done:
-            // the stages are free), then one 512-byte bulk store per row into the partials
+            // O^T of the group's rows straight from TMEM into the partials: a warp's store of one
+            // row covers 32 consecutive dimensions (128 contiguous bytes); the rows' slots were
+            // computed during the set-up
             if (ntiles > 0)
                 tc_fence_after();
-            float *orow = reinterpret_cast<float *>(smem);
             const float o_scale = p.v_scale * (1.0f / (float)(1 << C::kPShift));
 #pragma unroll
             for (int c = 0; c < RH; c += kLd) {
@@ -884,24 +890,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                     for (int r = 0; r < kLd; ++r)
                         o[r] = 0.f;
                 }
+                const long long *slots = reinterpret_cast<const long long *>(misc + C::kSlot);
 #pragma unroll
                 for (int rr = 0; rr < kLd; ++rr) {
                     const int r = r0 + c + rr;
-                    orow[r * kHeadDim + tau] = alpha_s[r] > 0.f ? o[rr] * o_scale : 0.f;
+                    if (r < R)
+                        p.part_o[slots[r] * kHeadDim + tau] = alpha_s[r] > 0.f ? o[rr] * o_scale : 0.f;
                 }
             }
-            fence_proxy_async_smem();
-            named_bar_sync(bar_id, 128);
             const int r = r0 + tid;
             if (tid < RH && r < R) {
-                const int jq = (row0 + r) / p.G, i = row0 + r - jq * p.G;
-                const long long slot = (long long)(w.tok0 + jq) * p.seg_max * p.H_q + (long long)w.g * p.H_q + h * p.G + i;
-                bulk_store_s2g(p.part_o + slot * kHeadDim, sbase + (uint32_t)(r * kHeadDim * 4), kHeadDim * 4);
-                bulk_commit_group();
+                const long long slot = reinterpret_cast<const long long *>(misc + C::kSlot)[r];
                 const float l = alpha_s[r] * (1.0f / (float)(1 << C::kPShift));
                 p.part_m[slot] = l > 0.f ? m_run[r] * 0.69314718055994531f : -CUDART_INF_F;
                 p.part_l[slot] = l;
-                bulk_wait_reads();
             }
         }
     }

@@ -109,27 +109,6 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
-// Bulk copy shared -> global (no tensor map): both addresses 16-byte aligned,
-// `bytes` a multiple of 16.  Tracked by this thread's bulk groups.
-__device__ __forceinline__ void bulk_store_s2g(void *gdst, uint32_t ssrc, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(gdst)),
-                 "r"(ssrc), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit_group()
-{
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-
-// Waits until every bulk group this thread committed has read its shared-memory
-// source (the writes themselves are complete by the end of the grid).
-__device__ __forceinline__ void bulk_wait_reads()
-{
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-
 // Prefetch of one tensor-map box into L2 (no shared memory, no barrier).
 __device__ __forceinline__ void tma_prefetch_l2_4d(const CUtensorMap *map, int x, int y, int z, int w)
 {
