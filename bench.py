@@ -581,10 +581,11 @@ def _e2e_serving(a, w, sk, torch, dev, q, kv, bt, lens, cu, use_plan, nsm, ws, r
     """A serving step through the public calls with the K/V cache resident in HBM
     (model state, as in a server): every step copies this step's inputs from pinned
     host memory -- Q, the new tokens' K and V, their cache slots, seq_lens,
-    cu_seqlens_q and the block table -- writes the new K/V into the cache
-    (sk_reshape_and_cache), runs plan + attention + merge, and copies out and lse
-    back.  The new tokens' K/V are the cache's own rows, so the cache is unchanged.
-    The step runs as one captured CUDA graph."""
+    cu_seqlens_q and the block table, packed in one staging buffer, so one copy --
+    writes the new K/V into the cache (sk_reshape_and_cache), runs plan + attention
+    + merge into one output buffer, and copies out and lse back in one copy.  The new
+    tokens' K/V are the cache's own rows, so the cache is unchanged.  The step runs as
+    one captured CUDA graph."""
     nt, hkv = w.num_tokens, w.num_kv_heads
     slots = np.concatenate([
         w.block_table[s, np.arange(int(w.seq_lens[s]) - int(w.q_lens[s]), int(w.seq_lens[s])) // w.page]
@@ -598,27 +599,42 @@ def _e2e_serving(a, w, sk, torch, dev, q, kv, bt, lens, cu, use_plan, nsm, ws, r
     if w.kv_dtype == si.KV_FP8:      # the step's K/V arrive in bf16 and are quantised by the write
         k_new = (k_new.view(torch.float8_e4m3fn).float() * w.k_scale).to(torch.bfloat16)
         v_new = (v_new.view(torch.float8_e4m3fn).float() * w.v_scale).to(torch.bfloat16)
-    host = {"q": q.cpu().pin_memory(), "k": k_new.cpu().pin_memory(), "v": v_new.cpu().pin_memory(),
-            "slots": st.cpu().pin_memory(), "lens": lens.cpu().pin_memory(), "cu": cu.cpu().pin_memory(),
-            "bt": bt.cpu().pin_memory()}
-    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
-    out_h = torch.empty((nt, w.num_q_heads, d), dtype=torch.bfloat16).pin_memory()
-    lse_h = torch.empty((nt, w.num_q_heads), dtype=torch.float32).pin_memory()
+    inputs = {"q": q, "k": k_new, "v": v_new, "slots": st, "lens": lens, "cu": cu, "bt": bt}
+
+    def packed(tensors, pinned):
+        """One byte buffer holding every tensor (256-byte aligned) and typed views into it."""
+        offs, total = {}, 0
+        for k, t in tensors.items():
+            offs[k] = total
+            total += (t.numel() * t.element_size() + 255) // 256 * 256
+        buf = torch.empty(max(total, 256), dtype=torch.uint8, device="cpu" if pinned else dev)
+        if pinned:
+            buf = buf.pin_memory()
+        views = {k: buf[offs[k]:offs[k] + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+                 for k, t in tensors.items()}
+        return buf, views
+    host_buf, host_in = packed(inputs, True)
+    for k, t in inputs.items():
+        host_in[k].copy_(t.cpu())
+    dev_buf, dev_in = packed(inputs, False)
+    outs = {"out": torch.empty((nt, w.num_q_heads, d), dtype=torch.bfloat16, device=dev),
+            "lse": torch.empty((nt, w.num_q_heads), dtype=torch.float32, device=dev)}
+    out_dbuf, out_d = packed(outs, False)
+    out_hbuf, out_h = packed(outs, True)
     wsp = {}
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+    h2d = host_buf.numel()
+    d2h = out_hbuf.numel()
 
     def step():
-        for k in host:
-            dev_in[k].copy_(host[k], non_blocking=True)
+        dev_buf.copy_(host_buf, non_blocking=True)
         sk.sk_reshape_and_cache(dev_in["k"], dev_in["v"], dev_in["slots"], kv, k_scale=w.k_scale, v_scale=w.v_scale)
         sk.sk_plan_cache_reset()
-        o, l = sk.paged_decode_attention(dev_in["q"], kv, dev_in["bt"], dev_in["lens"], dev_in["cu"],
-                                         max_q_len=w.max_q_len, sm_scale=w.sm_scale, num_sms=nsm,
-                                         k_scale=w.k_scale, v_scale=w.v_scale, causal=bool(w.causal),
-                                         seg_max=w.seg_max, use_plan=use_plan, workspace=wsp)
-        out_h.copy_(o, non_blocking=True)
-        lse_h.copy_(l, non_blocking=True)
+        sk.paged_decode_attention(dev_in["q"], kv, dev_in["bt"], dev_in["lens"], dev_in["cu"],
+                                  max_q_len=w.max_q_len, sm_scale=w.sm_scale, num_sms=nsm,
+                                  k_scale=w.k_scale, v_scale=w.v_scale, causal=bool(w.causal),
+                                  seg_max=w.seg_max, use_plan=use_plan, workspace=wsp,
+                                  out=out_d["out"], lse=out_d["lse"])
+        out_hbuf.copy_(out_dbuf, non_blocking=True)
 
     # the step is captured once as a CUDA graph (the calls are capture safe) and replayed,
     # as a server would run it: no per-call host work inside the timed region
@@ -647,11 +663,12 @@ def _e2e_serving(a, w, sk, torch, dev, q, kv, bt, lens, cu, use_plan, nsm, ws, r
     ms = max_over_ranks(e0.elapsed_time(e1), ws, dev)
     if sk.sk_get_device_status(clear=True):
         raise RuntimeError("device status set during the serving-step run")
-    assert torch.equal(out_h, ref_out.cpu()), "serving-step output differs from the device-resident run"
+    assert torch.equal(out_h["out"], ref_out.cpu()), "serving-step output differs from the device-resident run"
     return {"value": weak_scaling_tbps(w.kv_bytes, steps, ws, ms), "unit": "TB/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": ms / steps,
             "cache": "resident in HBM; each step writes its new tokens' K/V with sk_reshape_and_cache",
-            "launch": "one CUDA graph per step: H2D copies, KV write, plan, attention, merge, D2H copies"}
+            "launch": ("one CUDA graph per step: one H2D copy of the packed inputs, KV write, plan, attention, "
+                       "merge, one D2H copy of out and lse")}
 
 
 def run_kv_write(a, local):
