@@ -27,7 +27,10 @@
  *    sk_paged_decode_attention_static (both static __device__ variables).
  *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
  *    legacy default stream).  No call synchronises, so the whole path can be
- *    captured into a CUDA graph.
+ *    captured into a CUDA graph.  Every kernel is launched with programmatic
+ *    stream serialization: it may start while the kernel before it on the
+ *    stream finishes, and waits for that kernel's completion (and its writes)
+ *    before it reads anything, so stream order is kept.
  *  - Invalid arguments are caught on the host before anything is launched
  *    and return a negative sk_status; sk_last_error() then describes the
  *    problem.  Conditions only the device can see (a block id outside
