@@ -14,7 +14,7 @@
 // so that they stream the same pages at about the same time (L2 serves the
 // repeats).
 //
-// Roles (352 threads):
+// Roles (352 threads; 608 for fp8 with 64 rows, with four softmax warpgroups):
 //   warp 0   TMA producer: one 4-D copy per page (8 or 16 per tile) into
 //            128-byte-swizzled atoms that are at once the K-major K operand
 //            and the MN-major V^T operand (layout below).  Pages past the
@@ -22,9 +22,9 @@
 //            It starts as soon as the mbarriers exist, with the block ids of
 //            its first tiles already read; later it reads them a ring ahead.
 //   warp 1   allocates TMEM; issues the QK products.
-//   warp 10  issues the PV products.  Both issuers run converged and issue
+//   warp 10 (18)  issues the PV products.  Both issuers run converged and issue
 //            through one elected lane, so the descriptors stay warp-uniform.
-//   warps 2-9  softmax, two warpgroups: one thread per token of each 128-token
+//   warps 2-9 (2-17)  softmax, two (four) warpgroups: one thread per token of each 128-token
 //            half of the tile (its TMEM lane); warps 2-5 take the first half of
 //            the query rows, warps 6-9 the second, each group on its own.
 //            The running max per query row is kept lazily: scores are
@@ -36,9 +36,10 @@
 //            P^T is written over the tile's own K area, which QK no longer
 //            needs, so every stage carries its own P buffer.
 // fp8 pages: both products run as kind::f8f6f4 on the e4m3 codes as they
-// arrive, so a stage holds only codes: a 256-token tile (64 KB, three stages)
-// for up to 32 rows, whose single softmax pass covers as many bytes as a bf16
-// tile's, else a 128-token tile (32 KB, six stages).
+// arrive, so a stage holds only codes: a 256-token tile (64 KB, three stages),
+// whose single softmax pass covers as many bytes as a bf16 tile's.  With 64 rows
+// the rows are split over four softmax warpgroups (608 threads) instead of two,
+// so that a thread holds 16 rows of its two tokens.
 // QK splits Q into two e4m3 terms (q * 2^e_r = hi + lo, a power-of-two scale
 // per row): for up to 32 rows the two terms are one stacked operand (S_hi |
 // S_lo, added by the softmax), else two products into the same S.  PV splits
@@ -66,10 +67,6 @@ using namespace sm100;
 
 constexpr int kTokTile = 128;                       // tokens per MMA (M)
 constexpr int kSoftmaxWarp0 = 2;
-constexpr int kSoftmaxGroups = 2;                   // warpgroups splitting the query rows
-constexpr int kSoftmaxWarps = 4 * kSoftmaxGroups;
-constexpr int kPvWarp = kSoftmaxWarp0 + kSoftmaxWarps;   // 10: issues the PV products
-constexpr int kThreads = 32 * (kPvWarp + 1);        // 352
 constexpr long long kWaitLimit = 4000000000LL;      // cycles (~2 s)
 constexpr uint32_t kFull = 0xffffffffu;
 constexpr int kMaxSmem = 232448;                    // 227 KB per CTA
@@ -81,17 +78,22 @@ constexpr int kMaxSmem = 232448;                    // 227 KB per CTA
 // operand over 128 tokens whose 8-row groups are kGroupBytes apart.
 //   bf16: 128-token tiles, 64 KB stages, groups of 4 KB: chunks K 0-63 (later P^T),
 //         K 64-127, V 0-63, V 64-127
-//   fp8:  groups of 2 KB: chunks K codes (later P^T), V codes.  Up to 32 rows a tile is
-//         256 tokens (64 KB, two 128-token halves 32 KB apart), so the softmax's fixed
-//         cost per tile is spread over as many bytes as a bf16 tile; with 64 rows it is
-//         128 tokens (32 KB).
+//   fp8:  groups of 2 KB: chunks K codes (later P^T), V codes.  A tile is 256 tokens
+//         (64 KB, two 128-token halves 32 KB apart), so the softmax's fixed cost per tile
+//         is spread over as many bytes as a bf16 tile.
 template <int RP, bool FP8>
 struct Cfg {
     static_assert(RP == 16 || RP == 32 || RP == 64, "rows per work item: 16, 32 or 64");
     static constexpr int kQBytes = 2 * RP * 128;            // bf16: two 64-column chunks; fp8: hi and lo terms
-    static constexpr int kMiscBytes = 4096;
-    static constexpr int kRH = RP / kSoftmaxGroups;          // rows per softmax warpgroup
-    static constexpr int kTile = (FP8 && RP <= 32) ? 256 : 128;   // tokens per tile
+    static constexpr int kMiscBytes = 8192;
+    // Softmax warpgroups splitting the query rows: two, or four for fp8 with 64 rows, so
+    // that every softmax thread holds at most 16 rows of a 256-token fp8 tile's two tokens
+    static constexpr int kGroups = (FP8 && RP == 64) ? 4 : 2;
+    static constexpr int kSoftmaxWarps = 4 * kGroups;
+    static constexpr int kPvWarp = kSoftmaxWarp0 + kSoftmaxWarps;   // issues the PV products
+    static constexpr int kThreads = 32 * (kPvWarp + 1);      // 352, or 608
+    static constexpr int kRH = RP / kGroups;                  // rows per softmax warpgroup
+    static constexpr int kTile = FP8 ? 256 : 128;             // tokens per tile
     static constexpr int kHalves = kTile / kTokTile;          // 128-token MMAs per tile
     static constexpr int kPagesPerTile = kTile / kPage;       // TMA copies per tile (<= 32 lanes)
     static constexpr int kStageBytes = kTile * (FP8 ? 256 : 512);
@@ -133,7 +135,7 @@ struct Cfg {
     static constexpr int kTmemSlot = kBarODone + 8;
     static constexpr int kAbort = kTmemSlot + 4;
     static constexpr int kRed = 320;                         // float[group][4][32]
-    static constexpr int kMrun = kRed + kSoftmaxGroups * 4 * 32 * 4;   // float[64] running max (log2 units)
+    static constexpr int kMrun = kRed + kGroups * 4 * 32 * 4;   // float[64] running max (log2 units)
     static constexpr int kMthr = kMrun + 64 * 4;             // float[64] running max + rescale threshold
     static constexpr int kMsub = kMthr + 64 * 4;             // float[64] running max - kPShift, -inf -> 0
     static constexpr int kAlpha = kMsub + 64 * 4;            // float[64]; reused for the final l
@@ -237,7 +239,7 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 }
 
 template <int RP, bool FP8>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<RP, FP8>::kThreads, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
 {
     using C = Cfg<RP, FP8>;
@@ -291,8 +293,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
     // ---- set-up: barriers, TMEM, Q in shared memory (K-major, 128-byte swizzle)
     // Q is read into registers before the producer starts, so that its loads are not queued
     // behind every CTA's first copies.
-    constexpr uint32_t kSetupBar = 3;
-    constexpr int kSetupThreads = kThreads - 32;
+    constexpr uint32_t kSetupBar = 8;          // ids 1..kGroups belong to the softmax groups
+    constexpr int kSetupThreads = C::kThreads - 32;
     const int st_tid = threadIdx.x - 32;
     constexpr int kQUnits = FP8 ? (RP + kSetupThreads / 32 - 1) / (kSetupThreads / 32)   // rows per warp
                                 : (RP * 16 + kSetupThreads - 1) / kSetupThreads;         // 16-byte units per thread
@@ -343,8 +345,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
         }
         for (int b = 0; b < C::kSBufs; ++b) {
             mbar_init(bar_sfull(b), 1);
-            mbar_init(bar_sfree(b), kSoftmaxWarps);
-            mbar_init(bar_pfull(b), kSoftmaxWarps);
+            mbar_init(bar_sfree(b), C::kSoftmaxWarps);
+            mbar_init(bar_pfull(b), C::kSoftmaxWarps);
             mbar_init(bar_pvis(b), 1);
         }
         mbar_init(bar_odone, 1);
@@ -488,7 +490,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             for (int t = issued > C::kStages ? issued - C::kStages : 0; t < issued; ++t)
                 mbar_wait_bounded(bar_full(t % C::kStages), (t / C::kStages) & 1, nullptr, kWaitLimit);
         }
-    } else if (warp == 1 || warp == kPvWarp) {
+    } else if (warp == 1 || warp == C::kPvWarp) {
         // ================================================================ MMA issuers
         // Whole warps run these loops; one elected lane issues each MMA and commit.
         // QK: bf16 kind::f16, 8 steps of 16 dims; fp8 kind::f8f6f4, 4 steps of 32 dims, on the
@@ -820,11 +822,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                     const int tok = k0 + j * C::kTile + t;
                     if (tok >= w.L && tok < last_page_end) {
                         // past L in the last page the row holds anything (0 * NaN would reach O): this
-                        // group's half of the token's V row becomes zeros (bf16 chunk 2 + wg, fp8 64 bytes)
+                        // group's share of the token's V row becomes zeros (bf16: chunk 2 + wg; fp8: a
+                        // half or a quarter of the 128 code bytes)
+                        static_assert(FP8 || C::kGroups == 2, "bf16 V rows are zeroed by chunk");
+                        constexpr int kZeroBytes = FP8 ? 128 / C::kGroups : 128;
                         uint8_t *vrow = smem + st * C::kStageBytes + C::kOffV + (t >> 3) * C::kGroupBytes + (t & 7) * 128 +
-                                        wg * (FP8 ? 64 : 1024);
+                                        wg * (FP8 ? kZeroBytes : 1024);
 #pragma unroll
-                        for (int u = 0; u < (FP8 ? 4 : 8); ++u)
+                        for (int u = 0; u < kZeroBytes / 16; ++u)
                             *reinterpret_cast<uint4 *>(vrow + u * 16) = make_uint4(0u, 0u, 0u, 0u);
                     }
                 }
@@ -947,7 +952,8 @@ cudaError_t launch_rp(const CUtensorMap &map, const AttnParams &p, cudaStream_t 
     if (attr_err != cudaSuccess)
         return attr_err;
     const dim3 grid((unsigned)p.num_items * (unsigned)p.H_kv * (unsigned)p.row_blocks);
-    return launch_pdl(attn_tc_kernel<RP, FP8>, grid, dim3(kThreads), Cfg<RP, FP8>::kSmemBytes, stream, map, p);
+    return launch_pdl(attn_tc_kernel<RP, FP8>, grid, dim3(Cfg<RP, FP8>::kThreads), Cfg<RP, FP8>::kSmemBytes, stream,
+                      map, p);
 }
 
 }  // namespace
