@@ -2,7 +2,7 @@
 paged cache by sk_reshape_and_cache, then plan + split-KV attention + merge
 over that cache, against the oracle doing the same two steps.
 
-Two rounds: the whole history written at once (a prefill of the cache), then
+Two writes: the whole history written at once (a prefill of the cache), then
 each sequence's new query tokens appended (a verify step) and attended."""
 import math
 
@@ -52,12 +52,12 @@ def test_write_then_attend(kv_dtype, ks, vs):
                                        v_scale=vs) == sk.SK_OK
         oracle.reshape_and_cache(k_bits, v_bits, slots, ref_pages, kv_dtype, ks, vs)
 
-    # round 1: the history of every sequence
+    # first write: the history of every sequence
     slots = np.concatenate([_slots(bt, s, 0, int(hist[s])) for s in range(len(lens))])
     kh = to_bf16_bits(rng.normal(0, 1, (len(slots), hkv, D)))
     vh = to_bf16_bits(rng.normal(0, 1, (len(slots), hkv, D)))
     write(kh, vh, slots)
-    # round 2: this step's tokens, appended after each history
+    # second write: this step's tokens, appended after each history
     slots = np.concatenate([_slots(bt, s, int(hist[s]), int(lens[s])) for s in range(len(lens))])
     kn = to_bf16_bits(rng.normal(0, 1, (len(slots), hkv, D)))
     vn = to_bf16_bits(rng.normal(0, 1, (len(slots), hkv, D)))
