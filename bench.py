@@ -371,11 +371,14 @@ def run_sk(a, w, ws, rank, local):
     flush = None if w.kv_bytes > 129e6 else torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     flush_rd = None if flush is None else torch.ones(256 << 20, dtype=torch.uint8, device=dev)
     flush_sink = None if flush is None else torch.zeros(1, dtype=torch.int64, device=dev)
-    # The timed steps are captured once as a CUDA graph (every call is capture safe), with an
-    # event pair around each step recorded inside the graph, and replayed once: the device runs
-    # exactly the kernels of K eager steps, but the timing does not depend on how fast the host
-    # can issue the calls.  A second graph of the same steps, with events around each kernel,
-    # gives the per-kernel split.  --eager keeps the Python-launched loops.
+    # The timed steps are captured once as a CUDA graph (every call is capture safe) and replayed
+    # once: the device runs exactly the kernels of K eager steps, but the timing does not depend
+    # on how fast the host can issue the calls.  Inputs larger than L2 run the K steps back to
+    # back between one event pair (an event between two steps would cut the overlap of one
+    # step's last kernel with the next step's first launch, ~5 us per step); with the L2 flush,
+    # each step has its own pair, so the flushes stay out of the sum.  A second graph of the same
+    # steps, with events around each kernel, gives the per-kernel split.  --eager keeps the
+    # Python-launched loops.
     try:
         graph_events = not a.eager and torch.cuda.Event(enable_timing=True, external=True) is not None
     except TypeError:                      # a PyTorch without graph-recorded events
@@ -390,7 +393,7 @@ def run_sk(a, w, ws, rank, local):
         if flush is not None:
             flush.fill_(1)
             torch.sum(flush_rd.view(torch.int64), dim=0, keepdim=True, out=flush_sink)
-        if ev is not None:
+        if ev is not None and ev[0] is not None:
             ev[0].record(stream)
         if use_plan:
             sk.sk_plan_cache_reset()
@@ -404,8 +407,15 @@ def run_sk(a, w, ws, rank, local):
         if parts:
             ev[2].record(stream)
         sk.sk_merge_segments(part_o, part_m, part_l, tok, out, lse, fixed_nseg=fixed, stream=stream)
-        if ev is not None:
+        if ev is not None and ev[-1] is not None:
             ev[-1].record(stream)
+
+    def timed_events(i):
+        # the events step i of the timed run records: its own pair with the flush, else only
+        # the first step's start and the last step's end
+        if flush is not None:
+            return evs[i]
+        return [evs[0][0] if i == 0 else None, evs[-1][1] if i == a.steps - 1 else None]
 
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
@@ -425,7 +435,7 @@ def run_sk(a, w, ws, rank, local):
                     step()
             with torch.cuda.graph(g_timed, stream=stream):
                 for i in range(a.steps):
-                    step(evs[i])
+                    step(timed_events(i))
             with torch.cuda.graph(g_parts, stream=stream):
                 for i in range(a.steps):
                     step(evp[i])
@@ -447,7 +457,7 @@ def run_sk(a, w, ws, rank, local):
         g_timed.replay()
     else:
         for i in range(a.steps):
-            step(evs[i])
+            step(timed_events(i))
     torch.cuda.synchronize()
     if ws > 1:
         torch.distributed.barrier()
@@ -671,6 +681,19 @@ def _e2e_serving(a, w, sk, torch, dev, q, kv, bt, lens, cu, use_plan, nsm, ws, r
                        "merge, one D2H copy of out and lse")}
 
 
+def _back_to_back_ms(torch, f, steps):
+    """Mean ms per call of `steps` calls of f issued back to back on the current stream
+    between one event pair (inputs larger than L2, so no flush between calls)."""
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(steps):
+        f()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
 def run_kv_write(a, local):
     """The KV write step on a prefill-sized chunk: 65536 new tokens x 8 KV heads
     scattered into shuffled page rows (256 MB of bf16 K/V in, larger than L2)."""
@@ -698,15 +721,8 @@ def run_kv_write(a, local):
         raise RuntimeError("device status set by the KV write")
     sampler = ClockSampler(local)
     sampler.start()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.steps)]
-    torch.cuda.synchronize()
-    for e0, e1 in evs:
-        e0.record()
-        f()
-        e1.record()
-    torch.cuda.synchronize()
+    ms = _back_to_back_ms(torch, f, a.steps)
     clocks = sampler.stop()
-    ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
     moved = nt * hkv * (2 * d * 2 + 2 * d * (1 if fp8 else 2)) + nt * 8   # K/V in, page rows out, slots
     gbs = moved / (ms * 1e-3) / 1e9
     peak, kind = _peaks()
@@ -833,14 +849,8 @@ def run_shuffle(a, local):
         raise RuntimeError("device status set by the conversion")
     sampler = ClockSampler(local)
     sampler.start()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.steps)]
-    for e0, e1 in evs:
-        e0.record()
-        f()
-        e1.record()
-    torch.cuda.synchronize()
+    ms = _back_to_back_ms(torch, f, a.steps)
     clocks = sampler.stop()
-    ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
     moved = 2 * kv.numel() * kv.element_size()
     gbs = moved / (ms * 1e-3) / 1e9
     peak, kind = _peaks()

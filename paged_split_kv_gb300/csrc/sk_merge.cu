@@ -12,8 +12,10 @@
 // 64 segments into registers (lane i: segments i and i + 32), so M, the
 // segment weights and Lambda come out of one load round; the weighted sum of
 // the o vectors then runs over the warp's share of the segments, each lane
-// owning 4 of the 128 dimensions (one coalesced 512-byte read per segment),
-// with no load in the loop depending on another and up to eight in flight.
+// owning 4 of the 128 dimensions (one coalesced 512-byte read per segment).
+// The first 8 (one warp a row) or 16 (four) of a warp's o vectors are loaded
+// with the (m, l), so up to 64 segments cost one round trip to L2; further
+// loads in the loop depend on no other, up to eight in flight.
 // More than 64 segments take a strided path with the same arithmetic.  With
 // WPR = 4 the partial sums meet in shared memory.
 #include <cuda_bf16.h>
@@ -28,7 +30,6 @@ namespace {
 
 constexpr uint32_t kFull = 0xffffffffu;
 constexpr int kThreads = 128;
-constexpr int kPre = 8;            // o vectors a warp loads together with (m, l)
 
 __device__ __forceinline__ float seg_weight(float m, float l, float M)
 {
@@ -43,6 +44,9 @@ merge_kernel(const float *__restrict__ part_o, const float *__restrict__ part_m,
              float *__restrict__ lse)
 {
     constexpr int kRowsPerCta = (kThreads / 32) / WPR;
+    // o vectors a warp loads together with (m, l): with four warps a row, all 16 of a
+    // warp's segments when the fixed split gives 64
+    constexpr int kPre = WPR > 1 ? 16 : 8;
     __shared__ float4 acc_s[kThreads / 32][32];
     wait_prior_grid();    // the partials come from the attention kernel
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

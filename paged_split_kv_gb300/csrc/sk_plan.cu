@@ -14,6 +14,9 @@
 // The CTA has one warp per 32 sequences (at most 1024 threads); tile counts
 // sit in shared memory for batches up to kCacheSeqs, so a probe is one pass
 // over them and one barrier (partial sums double-buffered by probe parity).
+// A batch of at most 32 sequences is searched by its one warp 32 candidates
+// at a time (each lane sums the batch for its own T), two or three rounds
+// where bisection would take about log2 of the range.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -129,6 +132,29 @@ plan_kernel(const int32_t *__restrict__ seq_lens, const int32_t *__restrict__ cu
         // Every probe has mid >= S / B, so its total is below S / mid + bs <= B + bs < 2^32
         // (B < 2^31: plan_capacity > B is an int; bs < 2^15).
         // ceil(max / mid) <= seg_max is max <= seg_max * mid.
+        if (nwarps == 1) {
+            // One warp holds the whole batch (bs <= 32): each lane tests its own candidate,
+            // lo + l * step with the last one at hi, so every round cuts the range 31-fold.
+            // Feasibility is monotone, so the feasible lanes are a suffix and the first of
+            // them bounds T from above, its left neighbour from below.
+            const uint32_t my_t = tid < bs ? tiles_at(tid) : 0u;   // the sum is < 2^31 (bs <= 32, tiles < 2^26)
+            while (lo < hi) {
+                const long long step = (hi - lo + 30) / 31;
+                const long long c = lo + step * lane < hi ? lo + step * lane : hi;
+                const uint32_t c32 = (uint32_t)c;
+                uint32_t sum = 0;
+                for (int s = 0; s < bs; ++s)
+                    sum += (__shfl_sync(kFull, my_t, s) + c32 - 1u) / c32;
+                const bool ok = sum <= (uint32_t)budget && max_tiles <= (long long)seg_max * c;
+                const int k = __ffs(__ballot_sync(kFull, ok)) - 1;   // lane 31 tests hi: k >= 0
+                const long long c_k = lo + step * k < hi ? lo + step * k : hi;
+                if (k > 0)
+                    lo = lo + step * (k - 1) + 1;                  // lane k - 1 was below hi, infeasible
+                hi = c_k;
+                if (k == 0)
+                    lo = hi;
+            }
+        }
         int parity = 0;
         while (lo < hi) {
             const long long mid = lo + (hi - lo) / 2;
