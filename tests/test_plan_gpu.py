@@ -68,6 +68,30 @@ def test_plan_fuzz():
         _check(lens.astype(np.int32), q.astype(np.int32), kv, nsm, seg)
 
 
+def test_plan_one_warp_search():
+    """Batches of at most 32 sequences take the one-warp search (32 candidate T per
+    round); 33 take bisection.  Wide length ranges (up to 16M keys; the oracle scans
+    every T, so longer ones would take it minutes) make the search range long, so
+    most cases run several rounds."""
+    rng = np.random.default_rng(321)
+    for trial in range(400):
+        bs = 32 if trial % 10 == 0 else 33 if trial % 10 == 1 else int(rng.integers(1, 33))
+        kind = trial % 3
+        if kind == 0:
+            lens = np.exp(rng.uniform(0, np.log(16_000_000), size=bs))
+        elif kind == 1:
+            lens = rng.integers(0, 2_000_000, size=bs)
+        else:
+            lens = np.full(bs, int(rng.integers(1, 16_000_000)))
+            lens[rng.random(bs) < 0.3] = 0
+        lens = lens.astype(np.int64)
+        q = rng.integers(0, 4, size=bs)
+        kv = int(rng.choice([1, 2, 4, 8]))
+        nsm = int(rng.choice([148, 152, 40, 1000]))
+        seg = int(rng.choice([64, 16, 1, 300, 4096]))
+        _check(lens.astype(np.int32), q.astype(np.int32), kv, nsm, seg)
+
+
 def test_plan_capacity_above_minimum_is_padded_with_minus_one():
     lens = np.array([5000, 70000, 3], np.int32)
     plan, tok, cu, cap = _gpu_plan(lens, [4, 4, 4], 2, 148, 64, cap=300)
