@@ -604,6 +604,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
         // sums and P entries, so the two groups never wait for each other.
         constexpr int RH = C::kRH;
         constexpr int kLd = RH >= 32 ? 32 : RH;                // TMEM columns per load
+        static_assert(kLd % 4 == 0, "the epilogue transposes blocks of four rows");
         const int wg = (warp - kSoftmaxWarp0) >> 2;            // softmax group
         const int tw = (warp - kSoftmaxWarp0) & 3;             // warp within the group
         const int r0 = wg * RH;                                // first row of the group
@@ -763,6 +764,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                 // MN-major, 128-byte swizzle, 16-byte unit u of row t stored at u ^ (t % 8).
                 // bf16: row r at bytes [2r, 2r + 2).  fp8: p * 2^kPShift = hi + lo, two e4m3 codes
                 // at bytes r and RP + r.
+                // The group's running maxima are read before the first P store: the compiler cannot
+                // tell the stores from these shared-memory words, so a read after a store would
+                // wait for it (1-2 us per call on the large batches).
+                float msub[RH];
+#pragma unroll
+                for (int r = 0; r < RH; r += 4) {
+                    const float4 m4 = *reinterpret_cast<const float4 *>(m_sub + r0 + r);
+                    msub[r] = m4.x;
+                    msub[r + 1] = m4.y;
+                    msub[r + 2] = m4.z;
+                    msub[r + 3] = m4.w;
+                }
 #pragma unroll
                 for (int hf = 0; hf < NH; ++hf) {
                     const int t = hf * kTokTile + tau;          // token of the tile
@@ -770,9 +783,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                     uint2 hprev = make_uint2(0u, 0u), lprev = make_uint2(0u, 0u);
 #pragma unroll
                     for (int u = 0; u < RH / 8; ++u) {
-                        const float4 ma = *reinterpret_cast<const float4 *>(m_sub + r0 + 8 * u);
-                        const float4 mb = *reinterpret_cast<const float4 *>(m_sub + r0 + 8 * u + 4);
-                        const float mm[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
+                        const float *mm = msub + 8 * u;
                         uint32_t pk[4], hc[4], lc[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
@@ -869,9 +880,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
         // the group's verdict; the barrier also publishes the row sums written above
         const bool write = !named_bar_or(bar_id, 128, !okf);
         if (write) {
-            // O^T of the group's rows straight from TMEM into the partials: a warp's store of one
-            // row covers 32 consecutive dimensions (128 contiguous bytes); the rows' slots were
-            // computed during the set-up
+            // O^T of the group's rows straight from TMEM into the partials (a warp holds 32
+            // dimensions of each row); the rows' slots were computed during the set-up
             if (ntiles > 0)
                 tc_fence_after();
             const float o_scale = p.v_scale * (1.0f / (float)(1 << C::kPShift));
@@ -897,10 +907,29 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                 }
                 const long long *slots = reinterpret_cast<const long long *>(misc + C::kSlot);
 #pragma unroll
-                for (int rr = 0; rr < kLd; ++rr) {
-                    const int r = r0 + c + rr;
+                for (int rr = 0; rr < kLd; ++rr)
+                    o[rr] = alpha_s[r0 + c + rr] > 0.f ? o[rr] * o_scale : 0.f;
+                // 4 x 4 transposes within lane quads: lane 4a + b ends with row 4k + b of each block of
+                // four rows and dimensions 4a .. 4a + 3 of the warp's quarter, so a warp store writes
+                // four rows of 128 contiguous bytes, 16 bytes a lane (part_o is 16-byte aligned)
+                const int qb = lane & 3;
+                const bool qb0 = (qb & 1) != 0, qb1 = (qb & 2) != 0;
+                const int dim4 = quarter * 32 + (lane & ~3);
+#pragma unroll
+                for (int k = 0; k < kLd / 4; ++k) {
+                    const float x0 = o[4 * k], x1 = o[4 * k + 1], x2 = o[4 * k + 2], x3 = o[4 * k + 3];
+                    const float own0 = qb1 ? x2 : x0, own1 = qb1 ? x3 : x1;
+                    const float rc0 = __shfl_xor_sync(kFull, qb1 ? x0 : x2, 2);
+                    const float rc1 = __shfl_xor_sync(kFull, qb1 ? x1 : x3, 2);
+                    const float zl0 = qb1 ? rc0 : own0, zl1 = qb1 ? rc1 : own1;
+                    const float zh0 = qb1 ? own0 : rc0, zh1 = qb1 ? own1 : rc1;
+                    const float rl = __shfl_xor_sync(kFull, qb0 ? zl0 : zl1, 1);
+                    const float rh = __shfl_xor_sync(kFull, qb0 ? zh0 : zh1, 1);
+                    const float kl = qb0 ? zl1 : zl0, kh = qb0 ? zh1 : zh0;
+                    const float4 y = make_float4(qb0 ? rl : kl, qb0 ? kl : rl, qb0 ? rh : kh, qb0 ? kh : rh);
+                    const int r = r0 + c + 4 * k + qb;
                     if (r < R)
-                        p.part_o[slots[r] * kHeadDim + tau] = alpha_s[r] > 0.f ? o[rr] * o_scale : 0.f;
+                        *reinterpret_cast<float4 *>(p.part_o + slots[r] * kHeadDim + dim4) = y;
                 }
             }
             const int r = r0 + tid;
