@@ -34,7 +34,9 @@
 //            and O rescaled (which waits for the previous PV).
 //            Row sums are kept per thread and reduced once at the end.
 //            P^T is written over the tile's own K area, which QK no longer
-//            needs, so every stage carries its own P buffer.
+//            needs, so every stage carries its own P buffer.  At the end the
+//            same warps move O^T from TMEM into the partials, 16 bytes a lane
+//            after a transpose within lane quads.
 // fp8 pages: both products run as kind::f8f6f4 on the e4m3 codes as they
 // arrive, so a stage holds only codes: a 256-token tile (64 KB, three stages),
 // whose single softmax pass covers as many bytes as a bf16 tile's.  With 64 rows
