@@ -13,7 +13,7 @@ import torch
 
 import paged_split_kv_gb300 as sk
 import sk_inputs as si
-from gpu_helpers import (TOL_PLAN_VS_FIXED, oracle_problem, oracle_sampled, problem_tensors,
+from gpu_helpers import (TOL_BF16, TOL_PLAN_VS_FIXED, oracle_problem, oracle_sampled, problem_tensors,
                          run_library, segments_of, tol_for, host_bits)
 from helpers import KV_BF16, KV_FP8, build_problem, repermute
 from oracle import oracle
@@ -207,6 +207,39 @@ def test_full_workload_sampled_rows(idx):
     r2 = run_library(w, q, kv, use_plan=False)
     diff = (r2.out.float() - out).abs().max().item()
     assert diff <= TOL_PLAN_VS_FIXED, diff
+
+
+def test_maximum_batch_of_short_sequences():
+    """The largest batch the calls accept (32767 sequences) of short requests: lengths
+    0..40 with a fifth empty, q 1..2, 8/1 heads.  More non-empty sequences than the
+    plan's budget, so every sequence is one segment (about 26000 CTAs); sampled rows
+    against the oracle, every empty sequence's rows 0 with lse -inf, and the fixed
+    split (one segment) equal to the plan."""
+    rng = np.random.default_rng(32767)
+    bs = 32767
+    lens = rng.integers(0, 41, size=bs)
+    lens[rng.random(bs) < 0.2] = 0
+    w = si.make_workload("max_batch", lens, rng.integers(1, 3, size=bs), 8, 1, seed=97)
+    dev = torch.device(DEV)
+    q, kv, r = _run_workload(w, dev)
+    assert r.status == 0
+    out = r.out.float().cpu().numpy()
+    lse = r.lse.cpu().numpy()
+    assert np.isfinite(out).all()
+    empty_tok = np.repeat(w.seq_lens == 0, w.q_lens)
+    assert np.all(out[empty_tok] == 0.0) and np.all(np.isneginf(lse[empty_tok]))
+    seqs = sorted(set(int(x) for x in rng.integers(0, bs, size=40)) | {0, bs - 1})
+    worst = 0.0
+    for t, h, o, l in oracle_sampled(w, q, kv, seqs, 2, rng):
+        worst = max(worst, float(np.max(np.abs(out[t, h] - o))))
+        if np.isfinite(l):
+            assert abs(lse[t, h] - l) <= 1e-3
+        else:
+            assert np.isneginf(lse[t, h])
+    assert worst <= TOL_BF16, worst
+    r2 = run_library(w, q, kv, use_plan=False)
+    assert r2.status == 0
+    assert torch.equal(r2.out, r.out)
 
 
 @pytest.mark.parametrize("seq_len,bs,q,hq,hkv,kv_dtype", [
