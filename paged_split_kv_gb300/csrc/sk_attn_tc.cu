@@ -513,14 +513,19 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
         if (warp == 1) {
             // QK(j) once tile j has landed, its S buffer (j % kSBufs) is free, and PV(j - kSBufs)
             // is issued.  The last condition keeps barrier phases unambiguous: P_full[b] cannot
-            // run a full round of buffers ahead of its PV.
+            // run a full round of buffers ahead of its PV.  The two conditions on tile
+            // j - kSBufs are checked first, while tile j is still in flight, so that once it
+            // lands only its own wait stands before the products (an mbarrier check can take
+            // hundreds of cycles while the softmax warps keep shared memory busy: fp8
+            // draft-extend 202.2 -> 198.5 us per step).  Neither condition depends on tile j.
             for (int j = 0; j < ntiles && ok; ++j) {
                 const int st = j % C::kStages, b = j % C::kSBufs;
-                ok = mbar_wait_bounded(bar_full(st), (j / C::kStages) & 1, abort_flag, kWaitLimit);
-                if (ok && j >= C::kSBufs)
+                if (j >= C::kSBufs)
                     ok = mbar_wait_bounded(bar_sfree(b), ((j / C::kSBufs) - 1) & 1, abort_flag, kWaitLimit);
                 if (ok && j >= C::kSBufs)     // PV(j - kSBufs) issued: phase j / kSBufs - 1 of pvis[b]
                     ok = mbar_wait_bounded(bar_pvis(b), ((j / C::kSBufs) - 1) & 1, abort_flag, kWaitLimit);
+                if (ok)
+                    ok = mbar_wait_bounded(bar_full(st), (j / C::kStages) & 1, abort_flag, kWaitLimit);
                 ok = __all_sync(kFull, ok);
                 if (!ok)
                     break;
