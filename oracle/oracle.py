@@ -86,6 +86,8 @@ def _load():
         lib.sko_merge.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, P, P]
         lib.sko_num_threads.restype = i32
         lib.sko_num_threads.argtypes = []
+        lib.sko_set_num_threads.restype = None
+        lib.sko_set_num_threads.argtypes = [i32]
         _lib = lib
         return lib
 
@@ -101,6 +103,12 @@ def _c(a, dtype) -> np.ndarray:
 def num_threads() -> int:
     """Threads the oracle's parallel loops use."""
     return int(_load().sko_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads for the oracle's parallel loops (n <= 0: every processor).  For
+    timing only: every result is the same at any thread count."""
+    _load().sko_set_num_threads(int(n))
 
 
 def bf16_to_double(bits: int) -> float:

@@ -538,3 +538,14 @@ int sko_num_threads(void)
     return 1;
 #endif
 }
+
+/* Sets the thread count of the loops above (n <= 0: every processor); a no-op
+ * without OpenMP.  Timing only: the results do not depend on it. */
+void sko_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    omp_set_num_threads(n > 0 ? n : omp_get_num_procs());
+#else
+    (void)n;
+#endif
+}
