@@ -165,6 +165,7 @@ long long sk_plan_launch_count(void);
  *   score; m + log(l) and o / l are the segment's unique log-sum-exp and output.
  *   Arrays are [num_tokens, seg_max, num_q_heads(, head_dim)]; only segments
  *   that exist are written.
+ * q, kv_pages and part_o must be 16-byte aligned (SK_ERR_INVALID otherwise).
  * Returns SK_OK or a negative sk_status. */
 int sk_paged_decode_attn(const void *q, const void *kv_pages, int kv_dtype, float k_scale,
                          float v_scale, const int32_t *block_table, int block_table_stride,
@@ -184,6 +185,7 @@ int sk_paged_decode_attn(const void *q, const void *kv_pages, int kv_dtype, floa
  * No contributing segment: out = 0, lse = -inf.
  * out bf16 [num_tokens, num_q_heads, head_dim]; lse fp32 [num_tokens,
  * num_q_heads] or NULL.  Partials as written by sk_paged_decode_attn.
+ * part_o must be 16-byte and out 8-byte aligned (SK_ERR_INVALID otherwise).
  * Returns SK_OK or a negative sk_status. */
 int sk_merge_segments(const float *part_o, const float *part_m, const float *part_l,
                       const int32_t *tok_nseg, int fixed_nseg, int num_tokens, int num_q_heads,

@@ -79,6 +79,8 @@ def test_attention_rejects_bad_arguments_without_cuda(sklib):
     assert call(bs=0) == -1
     assert call(q=None) == -1
     assert call(q=ctypes.c_void_p(264)) == -1          # not 16-byte aligned
+    assert call(kv=ctypes.c_void_p(264)) == -1
+    assert call(po=ctypes.c_void_p(264)) == -1         # the epilogue stores 16 bytes a lane
     assert call(scale=0.0) == -1
     assert call(dt=1, ks=0.0) == -1
     assert call(mq=0) == -1                            # tokens but no query length
@@ -91,6 +93,8 @@ def test_merge_rejects_bad_arguments_without_cuda(sklib):
     assert f(FAKE, FAKE, FAKE, None, 65, 4, 8, 128, 64, FAKE, None, None) == -1
     assert f(FAKE, FAKE, FAKE, None, 1, 4, 8, 96, 64, FAKE, None, None) == -3
     assert f(None, FAKE, FAKE, None, 1, 4, 8, 128, 64, FAKE, None, None) == -1
+    assert f(ctypes.c_void_p(264), FAKE, FAKE, None, 1, 4, 8, 128, 64, FAKE, None, None) == -1   # part_o % 16
+    assert f(FAKE, FAKE, FAKE, None, 1, 4, 8, 128, 64, ctypes.c_void_p(260), None, None) == -1   # out % 8
 
 
 def test_kv_write_rejects_bad_arguments_without_cuda(sklib):
