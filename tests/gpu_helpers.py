@@ -123,6 +123,33 @@ def oracle_sampled(w, q, kv, seqs, rows_per_seq, rng):
     return res
 
 
+def oracle_all_rows(w, q, kv):
+    """Oracle output and lse of every (token, query head) row of workload ``w``
+    (small workloads: one oracle call per sequence).  Returns (out [NT, H_q, D],
+    lse [NT, H_q])."""
+    out = np.zeros((w.num_tokens, w.num_q_heads, w.head_dim))
+    lse = np.full((w.num_tokens, w.num_q_heads), -np.inf)
+    cu = w.cu_q
+    for s in range(w.bs):
+        L = int(w.seq_lens[s])
+        qs = int(w.q_lens[s])
+        if qs == 0:
+            continue
+        npg = (L + w.page - 1) // w.page
+        blocks = torch.as_tensor(w.block_table[s, :npg].astype(np.int64), device=kv.device)
+        kv_sub = kv.index_select(0, blocks) if npg else kv[:0]
+        q_bits, kv_bits = host_bits(q[cu[s]:cu[s] + qs], kv_sub, w.kv_dtype)
+        if npg == 0:
+            kv_bits = np.zeros((1,) + tuple(kv.shape[1:]), dtype=kv_bits.dtype)
+        bt = np.arange(max(npg, 1), dtype=np.int32)[None, :]
+        o, l = oracle.attention(q_bits, kv_bits, w.kv_dtype, w.k_scale, w.v_scale, bt, w.page,
+                                np.array([L], np.int32), np.array([0, qs], np.int32), w.num_q_heads,
+                                w.num_kv_heads, w.head_dim, w.sm_scale, w.causal)
+        out[cu[s]:cu[s] + qs] = o.reshape(qs, w.num_q_heads, w.head_dim)
+        lse[cu[s]:cu[s] + qs] = l.reshape(qs, w.num_q_heads)
+    return out, lse
+
+
 def segments_of(case, use_plan, num_sms=148, seg_max=64, tile=64):
     """(nseg, seg_tiles) per sequence from the oracle's own plan or fixed split."""
     lens = np.asarray(case.seq_lens, np.int32)

@@ -13,7 +13,8 @@ import torch
 
 import paged_split_kv_gb300 as sk
 import sk_inputs as si
-from gpu_helpers import (TOL_BF16, TOL_PLAN_VS_FIXED, oracle_problem, oracle_sampled, problem_tensors,
+from gpu_helpers import (TOL_BF16, TOL_PLAN_VS_FIXED, oracle_all_rows, oracle_problem, oracle_sampled,
+                         problem_tensors,
                          run_library, segments_of, tol_for, host_bits)
 from helpers import KV_BF16, KV_FP8, build_problem, repermute
 from oracle import oracle
@@ -206,6 +207,43 @@ def test_full_workload_sampled_rows(idx):
     # the planned and the fixed split agree on the same inputs
     r2 = run_library(w, q, kv, use_plan=False)
     diff = (r2.out.float() - out).abs().max().item()
+    assert diff <= TOL_PLAN_VS_FIXED, diff
+
+
+@pytest.mark.parametrize("use_plan", [True, False])
+def test_page_accuracy_shapes_elementwise(use_plan):
+    """The shapes of the page's accuracy tests, scaled down (GQA 16 and 8, agentic
+    skew with 0/1/5/17-token sequences, bs 1/2/24/64, ragged q 1..4 on e4m3 pages,
+    not causal): every output element and lse against the oracle, planned and
+    fixed split."""
+    dev = torch.device(DEV)
+    for w in si.small_cases():
+        q, kv, r = _run_workload(w, dev, use_plan=use_plan)
+        assert r.status == 0, w.name
+        ref, ref_lse = oracle_all_rows(w, q, kv)
+        got = r.out.float().cpu().numpy()
+        err = float(np.max(np.abs(got - ref), initial=0.0))
+        assert err <= tol_for(w.kv_dtype), (w.name, err)
+        lse = r.lse.cpu().numpy()
+        fin = np.isfinite(ref_lse)
+        assert np.array_equal(np.isneginf(lse), ~fin), w.name
+        assert np.max(np.abs(lse[fin] - ref_lse[fin]), initial=0.0) <= 1e-3, w.name
+
+
+def test_uniform_16x70k_sampled_rows():
+    """The page's uniform accuracy shape at full size: 16 sequences of 70000 keys,
+    q 4, GQA 16 (32/2 heads): sampled rows against the oracle, planned vs fixed."""
+    w = si.make_workload("uniform_16x70k", [70000] * 16, 4, 32, 2, seed=70)
+    dev = torch.device(DEV)
+    q, kv, r = _run_workload(w, dev)
+    assert r.status == 0
+    rng = np.random.default_rng(70)
+    samples = oracle_sampled(w, q, kv, sorted(set(int(x) for x in rng.integers(0, 16, size=4))), 4, rng)
+    got = r.out.float().cpu().numpy()
+    worst = max(float(np.max(np.abs(got[t, h] - o))) for t, h, o, _ in samples)
+    assert worst <= TOL_BF16, worst
+    r2 = run_library(w, q, kv, use_plan=False)
+    diff = (r2.out.float() - r.out.float()).abs().max().item()
     assert diff <= TOL_PLAN_VS_FIXED, diff
 
 
