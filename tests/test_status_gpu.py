@@ -41,3 +41,75 @@ def test_query_length_above_bound_is_reported():
     sk.sk_paged_decode_attn(q, kv, bt, lens, cu, None, po, pm, pl, max_q_len=3,
                             sm_scale=pr.sm_scale, num_sms=148)
     assert sk.sk_get_device_status(clear=True) & sk.SK_DEV_BAD_SEQ
+
+
+def _partials(nt, hq, seg_max=64):
+    return (torch.zeros((nt, seg_max, hq, 128), dtype=torch.float32, device=D),
+            torch.zeros((nt, seg_max, hq), dtype=torch.float32, device=D),
+            torch.zeros((nt, seg_max, hq), dtype=torch.float32, device=D))
+
+
+def test_corrupted_query_offsets_are_reported():
+    """cu_seqlens_q that runs backwards (sequence 1 would have -1 query tokens): the
+    plan and the attention report it, skip that sequence and touch nothing outside
+    their arrays; the next clean call reports nothing."""
+    pr = build_problem([100, 40, 60], [3, 1, 1], 8, 2, seed=53)
+    q, kv = problem_tensors(pr, D)
+    lens = torch.as_tensor(pr.seq_lens, device=D)
+    bt = torch.as_tensor(pr.block_table, device=D)
+    bad_cu = torch.tensor([0, 3, 2, 5], dtype=torch.int32, device=D)
+    assert q.shape[0] == 5
+    plan = torch.full((sk.plan_capacity(3, 2, 148),), -7, dtype=torch.int32, device=D)
+    tok = torch.zeros(5, dtype=torch.int32, device=D)
+    po, pm, pl = _partials(5, 8)
+    sk.sk_get_device_status(clear=True)
+    sk.sk_plan_cache_reset()
+    sk.sk_build_plan(lens, bad_cu, 2, plan, tok, 148, 64)
+    torch.cuda.synchronize()
+    assert sk.sk_get_device_status(clear=True) & sk.SK_DEV_BAD_SEQ
+    sk.sk_paged_decode_attn(q, kv, bt, lens, bad_cu, plan, po, pm, pl, max_q_len=3,
+                            sm_scale=pr.sm_scale, num_sms=148)
+    assert sk.sk_get_device_status(clear=True) & sk.SK_DEV_BAD_SEQ
+    assert torch.isfinite(po).all()
+    r = run_library(pr, q, kv)
+    assert r.status == 0
+
+
+def test_sequence_longer_than_its_block_table_row_is_reported():
+    """A length past block_table_stride * page: the item is skipped and reported."""
+    pr = build_problem([100, 40], 1, 8, 2, seed=54)
+    q, kv = problem_tensors(pr, D)
+    bt = torch.as_tensor(pr.block_table, device=D)
+    long_lens = torch.tensor([bt.shape[1] * 16 + 1, 40], dtype=torch.int32, device=D)
+    cu = torch.as_tensor(pr.cu_q, device=D)
+    po, pm, pl = _partials(pr.num_tokens, 8)
+    sk.sk_get_device_status(clear=True)
+    sk.sk_paged_decode_attn(q, kv, bt, long_lens, cu, None, po, pm, pl, max_q_len=1,
+                            sm_scale=pr.sm_scale, num_sms=148)
+    assert sk.sk_get_device_status(clear=True) & sk.SK_DEV_BAD_SEQ
+    assert run_library(pr, q, kv).status == 0
+
+
+def test_plan_entries_out_of_range_are_reported():
+    """A caller-written plan naming a sequence past bs and a segment past seg_max:
+    those items are skipped and reported; the valid item still runs."""
+    pr = build_problem([100, 40], 1, 8, 2, seed=55)
+    q, kv = problem_tensors(pr, D)
+    lens = torch.as_tensor(pr.seq_lens, device=D)
+    cu = torch.as_tensor(pr.cu_q, device=D)
+    bt = torch.as_tensor(pr.block_table, device=D)
+    cap = sk.plan_capacity(2, 2, 148)
+    plan = torch.full((cap,), -1, dtype=torch.int32, device=D)
+    plan[0] = 2                                   # two tiles per segment
+    plan[1] = (5 << 16) | 0                       # sequence 5 of a batch of 2
+    plan[2] = (0 << 16) | 70                      # segment 70 >= seg_max
+    plan[3] = (1 << 16) | 0                       # sequence 1, segment 0: valid
+    po, pm, pl = _partials(pr.num_tokens, 8)
+    pl.fill_(-3.0)
+    sk.sk_get_device_status(clear=True)
+    sk.sk_paged_decode_attn(q, kv, bt, lens, cu, plan, po, pm, pl, max_q_len=1,
+                            sm_scale=pr.sm_scale, num_sms=148)
+    assert sk.sk_get_device_status(clear=True) & sk.SK_DEV_BAD_SEQ
+    # the valid item wrote its rows: sequence 1 is token 1, segment 0, query heads 0..7
+    assert torch.all(pl[1, 0] > 0)
+    assert run_library(pr, q, kv).status == 0
