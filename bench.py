@@ -587,8 +587,9 @@ def run_sk(a, w, ws, rank, local):
             "frac_of_8tbps_nominal": round(value / 8.0, 4),
             "roofline": roofline, "clocks": clocks, "e2e": e2e, "e2e_serving": e2e_serving, "cpu_baseline": cpu,
             "gpu_launches": a.steps * (3 if use_plan else 2),
-            "launch": ("timed steps replayed as one CUDA graph (events around each step; the per-kernel split "
-                       "comes from a second replay with events around each kernel)") if graph_events
+            "launch": ("timed steps replayed as one CUDA graph (one event pair around the back-to-back steps, "
+                       "or around each step when L2 is flushed between steps; the per-kernel split comes from a "
+                       "second replay with events around each kernel)") if graph_events
                       else "eager, one Python call per kernel"}
     print(json.dumps(line), flush=True)
     if ws > 1:
