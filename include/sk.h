@@ -35,8 +35,12 @@
  *    and return a negative sk_status; sk_last_error() then describes the
  *    problem.  Conditions only the device can see (a block id outside
  *    [0, num_blocks), a query length above max_q_len, an inconsistent
- *    cu_seqlens_q) set bits in the device status word and the affected work
- *    is skipped; read them with sk_get_device_status().
+ *    cu_seqlens_q, a wait that timed out) set bits in the device status word
+ *    and the affected work is skipped; read them with sk_get_device_status().
+ *    cu_seqlens_q must be non-decreasing with cu[0] == 0 and cu[bs] ==
+ *    num_tokens; otherwise SK_DEV_BAD_SEQ is set, tokens outside [cu[0],
+ *    cu[bs]) get 0 segments from the plan (output 0, lse -inf), and on the
+ *    fixed split their outputs are undefined.
  *  - Supported shapes: head_dim == 128, page_size == 16, 1 <= bs <= 32767
  *    (so seq << 16 stays positive), num_q_heads % num_kv_heads == 0.
  */
@@ -57,7 +61,7 @@ typedef enum {
     SK_ERR_CAPACITY = -2,     /* plan_capacity too small */
     SK_ERR_UNSUPPORTED = -3,  /* shape outside the supported set */
     SK_ERR_CUDA = -4,         /* a CUDA runtime call failed */
-    SK_ERR_TIMEOUT = -5       /* reserved: a device wait gave up */
+    SK_ERR_TIMEOUT = -5       /* sk_get_device_status: a bounded wait inside a kernel expired */
 } sk_status;
 
 typedef enum {
@@ -77,6 +81,14 @@ typedef enum {
  * tokens (SGLang PR 39172, Modifications: "tiles per segment come from
  * plan[0]").  Returns 64. */
 int sk_tile_tokens(void);
+
+/* Smallest valid plan_capacity for a batch: 1 + max(B, bs) with
+ * B = floor(num_sms / num_kv_heads), the plan's budget of work items (SGLang PR
+ * 39172, Modifications: total segments capped at num_CUs / kv_heads; a batch
+ * with more non-empty sequences than B takes one segment each, so up to bs
+ * items).  Host-only arithmetic; SK_ERR_INVALID for bs outside [1, 32767] or
+ * a non-positive head or SM count. */
+int sk_plan_capacity(int bs, int num_kv_heads, int num_sms);
 
 /* Segment count of the fixed split (SGLang PR 39172, Motivation):
  * max(1, min(seg_max, pow2floor(num_sms / (bs * num_kv_heads)))), pow2floor
@@ -100,7 +112,8 @@ int sk_fixed_nseg(int bs, int num_kv_heads, int num_sms, int seg_max);
  * Inputs (device): seq_lens int32[bs] (KV length including this step's query
  *   tokens), cu_seqlens_q int32[bs+1] (query-token offsets, cu[bs] ==
  *   num_tokens).
- * plan_capacity must be >= 1 + max(B, bs); larger values are allowed.
+ * plan_capacity must be >= sk_plan_capacity(bs, num_kv_heads, num_sms) =
+ * 1 + max(B, bs); larger values are allowed.
  *
  * Plan cache: the plan is built once per forward and reused by every layer.
  * The cache key is (seq_lens, seq_lens_version, cu_seqlens_q,
@@ -275,10 +288,32 @@ int sk_paged_decode_attention_static(const void *q, const void *kv_pages, int kv
  * sk_paged_decode_attention_static. */
 size_t sk_static_scratch_bytes(void);
 
-/* Synchronise `stream`, return the device status word of the current device
- * (a mask of SK_DEV_* bits, 0 when clean) and clear it when `clear` != 0.
- * Returns a negative sk_status if a CUDA call fails. */
+/* Synchronise `stream`, read the device status word of the current device
+ * and clear it when `clear` != 0.
+ * Returns SK_ERR_TIMEOUT when SK_DEV_TIMEOUT is set (a bounded wait expired and
+ * its work item was abandoned, so some partials and outputs of the calls since
+ * the last clear are missing); otherwise the mask of SK_DEV_* bits, 0 when
+ * clean; another negative sk_status if a CUDA call fails.  The whole mask read
+ * by the last call on this thread, timeout bit included, is
+ * sk_last_device_status(). */
 int sk_get_device_status(void *stream, int clear);
+
+/* The mask of SK_DEV_* bits that the last sk_get_device_status call on this
+ * thread read (0 before the first call). */
+int sk_last_device_status(void);
+
+/* Limit, in SM clock cycles, of each wait of the attention kernel that can
+ * give up (for a copy to land, a product to complete, another role to finish
+ * its part of a tile).  It applies to the launches made after the call;
+ * cycles < 0 restores the default of 4e9 (about two seconds).  Returns the
+ * previous limit.  Waits for work a CTA has already issued -- its copies and
+ * products in flight, before the CTA exits -- keep the default whatever this
+ * limit is.  This is a test hook: a limit far below the memory latency makes
+ * waits expire in an unchanged kernel, so the timeout path (SK_DEV_TIMEOUT,
+ * then SK_ERR_TIMEOUT from sk_get_device_status) can be exercised without
+ * faulting or hanging anything.  Process-wide; not for concurrent use with
+ * other calls. */
+long long sk_set_wait_limit(long long cycles);
 
 /* Message for the last negative status returned on this thread. */
 const char *sk_last_error(void);

@@ -20,13 +20,15 @@ from typing import Optional, Tuple
 __all__ = [
     "SkError", "lib", "sk_tile_tokens", "sk_fixed_nseg", "sk_build_plan", "sk_plan_cache_reset",
     "sk_plan_launch_count", "sk_paged_decode_attn", "sk_merge_segments", "sk_get_device_status",
-    "paged_decode_attention", "plan_capacity", "sk_paged_decode_attention_static",
-    "sk_static_scratch_bytes", "sk_reshape_and_cache", "sk_std_to_shuffled", "SK_OK", "SK_CACHED",
-    "SK_KV_BF16", "SK_KV_FP8_E4M3", "SK_DEV_BAD_BLOCK", "SK_DEV_BAD_SEQ", "SK_DEV_TIMEOUT",
+    "paged_decode_attention", "plan_capacity", "sk_plan_capacity", "sk_paged_decode_attention_static",
+    "sk_static_scratch_bytes", "sk_reshape_and_cache", "sk_std_to_shuffled", "sk_set_wait_limit",
+    "SK_OK", "SK_CACHED", "SK_ERR_TIMEOUT", "SK_KV_BF16", "SK_KV_FP8_E4M3", "SK_DEV_BAD_BLOCK",
+    "SK_DEV_BAD_SEQ", "SK_DEV_TIMEOUT",
 ]
 
 SK_OK = 0
 SK_CACHED = 1
+SK_ERR_TIMEOUT = -5
 SK_KV_BF16 = 0
 SK_KV_FP8_E4M3 = 1
 SK_DEV_BAD_BLOCK = 0x1
@@ -57,6 +59,12 @@ def lib():
         L.sk_tile_tokens.argtypes = []
         L.sk_fixed_nseg.restype = i32
         L.sk_fixed_nseg.argtypes = [i32, i32, i32, i32]
+        L.sk_plan_capacity.restype = i32
+        L.sk_plan_capacity.argtypes = [i32, i32, i32]
+        L.sk_set_wait_limit.restype = ctypes.c_longlong
+        L.sk_set_wait_limit.argtypes = [ctypes.c_longlong]
+        L.sk_last_device_status.restype = i32
+        L.sk_last_device_status.argtypes = []
         L.sk_build_plan.restype = i32
         L.sk_build_plan.argtypes = [P, u64, P, u64, i32, i32, i32, i32, i32, P, i32, P, P]
         L.sk_plan_cache_reset.restype = None
@@ -106,17 +114,44 @@ def _stream(stream) -> Optional[int]:
 
 
 def _need(t, dtype, name, dims=None):
-    import torch
+    """Type, layout and rank of one argument (where it lives is checked by _on_cuda)."""
     if t is None:
         raise ValueError(f"{name} is required")
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
     if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
         raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dims is not None and t.dim() != dims:
         raise ValueError(f"{name} must have {dims} dimensions, has {t.dim()}")
+
+
+def _shape(t, shape, name):
+    if t is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _on_cuda(**tensors):
+    for name, t in tensors.items():
+        if t is not None and not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+
+
+def _check_batch(q, kv_pages, block_table, seq_lens, cu_seqlens_q):
+    """The shapes an attention call reads through raw pointers: q [NT, H_q, D], kv_pages
+    [NB, H_kv, page, 2D] with H_kv dividing H_q, seq_lens [bs], cu_seqlens_q [bs + 1] and at
+    least bs block-table rows.  Returns (nt, hq, d, nb, hkv, page, bs)."""
+    nt, hq, d = q.shape
+    nb, hkv, page, d2 = kv_pages.shape
+    if d2 != 2 * d:
+        raise ValueError(f"kv_pages last dimension is {d2}, expected 2 * head_dim = {2 * d}")
+    if hkv < 1 or hq % hkv != 0:
+        raise ValueError(f"{hq} query heads are not a multiple of {hkv} KV heads")
+    bs = seq_lens.numel()
+    if cu_seqlens_q.numel() != bs + 1:
+        raise ValueError(f"cu_seqlens_q has {cu_seqlens_q.numel()} entries, expected bs + 1 = {bs + 1}")
+    if block_table.shape[0] < bs:
+        raise ValueError(f"block_table has {block_table.shape[0]} rows for {bs} sequences")
+    return nt, hq, d, nb, hkv, page, bs
 
 
 def sk_tile_tokens() -> int:
@@ -127,9 +162,19 @@ def sk_fixed_nseg(bs: int, num_kv_heads: int, num_sms: int, seg_max: int = 64) -
     return lib().sk_fixed_nseg(bs, num_kv_heads, num_sms, seg_max)
 
 
-def plan_capacity(bs: int, num_kv_heads: int, num_sms: int) -> int:
-    """Smallest valid plan buffer: 1 + max(floor(num_sms / num_kv_heads), bs)."""
-    return 1 + max(num_sms // num_kv_heads, bs)
+def sk_plan_capacity(bs: int, num_kv_heads: int, num_sms: int) -> int:
+    """Smallest valid plan buffer length for a batch (computed by the library)."""
+    return _check(lib().sk_plan_capacity(int(bs), int(num_kv_heads), int(num_sms)), "sk_plan_capacity")
+
+
+plan_capacity = sk_plan_capacity
+
+
+def sk_set_wait_limit(cycles: int) -> int:
+    """Sets the attention kernel's abortable-wait limit in SM cycles (negative:
+    the default, about two seconds) for later launches; returns the previous one.
+    A test hook for the timeout path."""
+    return int(lib().sk_set_wait_limit(int(cycles)))
 
 
 def sk_plan_cache_reset() -> None:
@@ -149,6 +194,9 @@ def sk_build_plan(seq_lens, cu_seqlens_q, num_kv_heads: int, plan, tok_nseg, num
     _need(plan, torch.int32, "plan", 1)
     _need(tok_nseg, torch.int32, "tok_nseg", 1)
     bs = seq_lens.numel()
+    if cu_seqlens_q.numel() != bs + 1:
+        raise ValueError(f"cu_seqlens_q has {cu_seqlens_q.numel()} entries, expected bs + 1 = {bs + 1}")
+    _on_cuda(seq_lens=seq_lens, cu_seqlens_q=cu_seqlens_q, plan=plan, tok_nseg=tok_nseg)
     rc = lib().sk_build_plan(_ptr(seq_lens), seq_lens._version, _ptr(cu_seqlens_q),
                              cu_seqlens_q._version, bs, tok_nseg.numel(), num_kv_heads, num_sms,
                              seg_max, _ptr(plan), plan.numel(), _ptr(tok_nseg), _stream(stream))
@@ -179,14 +227,13 @@ def sk_paged_decode_attn(q, kv_pages, block_table, seq_lens, cu_seqlens_q, plan,
     _need(part_l, torch.float32, "part_l", 3)
     if plan is not None:
         _need(plan, torch.int32, "plan", 1)
-    nt, hq, d = q.shape
-    nb, hkv, page, d2 = kv_pages.shape
-    if d2 != 2 * d:
-        raise ValueError("kv_pages last dimension must be 2 * head_dim")
+    nt, hq, d, nb, hkv, page, bs = _check_batch(q, kv_pages, block_table, seq_lens, cu_seqlens_q)
     seg_max = part_o.shape[1]
-    if tuple(part_o.shape) != (nt, seg_max, hq, d) or tuple(part_m.shape) != (nt, seg_max, hq) \
-            or tuple(part_l.shape) != (nt, seg_max, hq):
-        raise ValueError("partials must be [num_tokens, seg_max, num_q_heads(, head_dim)]")
+    _shape(part_o, (nt, seg_max, hq, d), "part_o")
+    _shape(part_m, (nt, seg_max, hq), "part_m")
+    _shape(part_l, (nt, seg_max, hq), "part_l")
+    _on_cuda(q=q, kv_pages=kv_pages, block_table=block_table, seq_lens=seq_lens, cu_seqlens_q=cu_seqlens_q,
+             plan=plan, part_o=part_o, part_m=part_m, part_l=part_l)
     rc = lib().sk_paged_decode_attn(
         _ptr(q), _ptr(kv_pages), _kv_dtype(kv_pages), float(k_scale), float(v_scale),
         _ptr(block_table), block_table.shape[1], nb, page, _ptr(seq_lens), _ptr(cu_seqlens_q),
@@ -208,6 +255,13 @@ def sk_merge_segments(part_o, part_m, part_l, tok_nseg, out, lse=None, fixed_nse
     if lse is not None:
         _need(lse, torch.float32, "lse", 2)
     nt, seg_max, hq, d = part_o.shape
+    _shape(part_m, (nt, seg_max, hq), "part_m")
+    _shape(part_l, (nt, seg_max, hq), "part_l")
+    _shape(out, (nt, hq, d), "out")
+    _shape(lse, (nt, hq), "lse")
+    if tok_nseg is not None and tok_nseg.numel() != nt:
+        raise ValueError(f"tok_nseg has {tok_nseg.numel()} entries for {nt} tokens")
+    _on_cuda(part_o=part_o, part_m=part_m, part_l=part_l, tok_nseg=tok_nseg, out=out, lse=lse)
     rc = lib().sk_merge_segments(_ptr(part_o), _ptr(part_m), _ptr(part_l), _ptr(tok_nseg),
                                  int(fixed_nseg), nt, hq, d, seg_max, _ptr(out), _ptr(lse),
                                  _stream(stream))
@@ -230,6 +284,7 @@ def sk_reshape_and_cache(key, value, slot_mapping, kv_pages, *, k_scale: float =
     nb, hkv2, page, d2 = kv_pages.shape
     if hkv2 != hkv or d2 != 2 * d:
         raise ValueError("kv_pages must be [num_blocks, num_kv_heads, page, 2 * head_dim]")
+    _on_cuda(key=key, value=value, slot_mapping=slot_mapping, kv_pages=kv_pages)
     rc = lib().sk_reshape_and_cache(_ptr(key), _ptr(value), _ptr(slot_mapping), nt, hkv, d,
                                     _ptr(kv_pages), _kv_dtype(kv_pages), float(k_scale), float(v_scale),
                                     nb, page, _stream(stream))
@@ -251,6 +306,7 @@ def sk_std_to_shuffled(kv_pages, k_shuf, v_shuf, block_ids=None, stream=None) ->
     x = 16 // kv_pages.element_size()
     if tuple(k_shuf.shape) != (nb, hkv, d // x, page, x) or tuple(v_shuf.shape) != (nb, hkv, page // x, d, x):
         raise ValueError("k_shuf must be [NB, H, D/x, page, x] and v_shuf [NB, H, page/x, D, x]")
+    _on_cuda(kv_pages=kv_pages, k_shuf=k_shuf, v_shuf=v_shuf, block_ids=block_ids)
     rc = lib().sk_std_to_shuffled(_ptr(kv_pages), _kv_dtype(kv_pages), _ptr(block_ids),
                                   0 if block_ids is None else block_ids.numel(), nb, hkv, d, page,
                                   _ptr(k_shuf), _ptr(v_shuf), _stream(stream))
@@ -264,10 +320,13 @@ def sk_static_scratch_bytes() -> int:
 def sk_paged_decode_attention_static(q, kv_pages, block_table, seq_lens, cu_seqlens_q, out, lse=None,
                                      *, max_q_len: int, sm_scale: float, num_sms: int,
                                      k_scale: float = 1.0, v_scale: float = 1.0, causal: bool = True,
-                                     seg_max: int = 64, use_plan: bool = True, stream=None) -> int:
+                                     seg_max: int = 64, use_plan: Optional[bool] = None,
+                                     stream=None) -> int:
     """The whole call without device allocation: plan, per-token counts and
     partials live in the library's fixed 32 MiB device array.  For callers that
-    cannot allocate; calls that overlap on the GPU race on that array."""
+    cannot allocate; calls that overlap on the GPU race on that array.
+    use_plan defaults to bs > 1, as in paged_decode_attention (bs == 1 takes the
+    fixed split)."""
     import torch
     _need(q, torch.bfloat16, "q", 3)
     _need(kv_pages, None, "kv_pages", 4)
@@ -277,8 +336,13 @@ def sk_paged_decode_attention_static(q, kv_pages, block_table, seq_lens, cu_seql
     _need(out, torch.bfloat16, "out", 3)
     if lse is not None:
         _need(lse, torch.float32, "lse", 2)
-    nt, hq, d = q.shape
-    nb, hkv, page, _ = kv_pages.shape
+    nt, hq, d, nb, hkv, page, bs = _check_batch(q, kv_pages, block_table, seq_lens, cu_seqlens_q)
+    _shape(out, (nt, hq, d), "out")
+    _shape(lse, (nt, hq), "lse")
+    if use_plan is None:
+        use_plan = bs > 1
+    _on_cuda(q=q, kv_pages=kv_pages, block_table=block_table, seq_lens=seq_lens, cu_seqlens_q=cu_seqlens_q,
+             out=out, lse=lse)
     rc = lib().sk_paged_decode_attention_static(
         _ptr(q), _ptr(kv_pages), _kv_dtype(kv_pages), float(k_scale), float(v_scale),
         _ptr(block_table), block_table.shape[1], nb, page, _ptr(seq_lens), _ptr(cu_seqlens_q),
@@ -288,7 +352,14 @@ def sk_paged_decode_attention_static(q, kv_pages, block_table, seq_lens, cu_seql
 
 
 def sk_get_device_status(stream=None, clear: bool = True) -> int:
-    return _check(lib().sk_get_device_status(_stream(stream), 1 if clear else 0), "sk_get_device_status")
+    """Synchronises and returns the mask of SK_DEV_* bits (0 when clean), the
+    timeout bit included: the C call reports a timeout as SK_ERR_TIMEOUT and
+    keeps the mask for sk_last_device_status()."""
+    L = lib()
+    rc = L.sk_get_device_status(_stream(stream), 1 if clear else 0)
+    if rc == SK_ERR_TIMEOUT:
+        return int(L.sk_last_device_status())
+    return _check(rc, "sk_get_device_status")
 
 
 def paged_decode_attention(q, kv_pages, block_table, seq_lens, cu_seqlens_q, *, max_q_len: int,

@@ -116,6 +116,22 @@ std::atomic<long long> g_plan_launches{0};
 
 int device_status_word(int **out) { return status_ptr(out); }
 
+namespace {
+std::atomic<long long> g_wait_limit{kDefaultWaitLimit};
+thread_local int g_last_device_status = 0;
+
+// Plan buffer length: the plan's T, then up to max(B, bs) work items, B = floor(num_sms /
+// num_kv_heads) (SGLang PR 39172, Modifications: the total segment count is capped at
+// num_CUs / kv_heads, and a batch with more non-empty sequences than that takes one each).
+long long capacity_of(int bs, int num_kv_heads, int num_sms)
+{
+    const long long budget = (long long)num_sms / num_kv_heads;
+    return 1 + (budget > bs ? budget : bs);
+}
+}  // namespace
+
+long long wait_limit() { return g_wait_limit.load(); }
+
 int set_error(int code, const char *msg) { return fail(code, "%s", msg); }
 
 }  // namespace sk
@@ -143,6 +159,24 @@ int sk_fixed_nseg(int bs, int num_kv_heads, int num_sms, int seg_max)
 
 const char *sk_last_error(void) { return g_msg; }
 
+int sk_plan_capacity(int bs, int num_kv_heads, int num_sms)
+{
+    if (bs < 1 || bs > 32767 || num_kv_heads < 1 || num_sms < 1)
+        return fail(SK_ERR_INVALID, "sk_plan_capacity: bs=%d num_kv_heads=%d num_sms=%d", bs, num_kv_heads,
+                    num_sms);
+    const long long c = capacity_of(bs, num_kv_heads, num_sms);
+    if (c > 0x7FFFFFFFLL)
+        return fail(SK_ERR_INVALID, "sk_plan_capacity: capacity overflows int");
+    return (int)c;
+}
+
+long long sk_set_wait_limit(long long cycles)
+{
+    return g_wait_limit.exchange(cycles < 0 ? kDefaultWaitLimit : cycles);
+}
+
+int sk_last_device_status(void) { return g_last_device_status; }
+
 void sk_plan_cache_reset(void)
 {
     std::lock_guard<std::mutex> lock(g_cache_mutex);
@@ -169,8 +203,7 @@ int sk_build_plan(const int32_t *seq_lens, uint64_t seq_lens_version, const int3
     if (seg_max < 1 || seg_max > 0xFFFF)
         return fail(SK_ERR_INVALID, "sk_build_plan: seg_max=%d outside [1, 65535]", seg_max);
     const int budget = num_sms / num_kv_heads;
-    const int need = 1 + (budget > bs ? budget : bs);
-    if (plan_capacity < need)
+    if (plan_capacity < capacity_of(bs, num_kv_heads, num_sms))
         return fail(SK_ERR_CAPACITY, "sk_build_plan: plan_capacity=%d < 1 + max(B=%d, bs=%d)",
                     plan_capacity, budget, bs);
 
@@ -220,13 +253,18 @@ int sk_build_plan(const int32_t *seq_lens, uint64_t seq_lens_version, const int3
     return SK_OK;
 }
 
-int sk_paged_decode_attn(const void *q, const void *kv_pages, int kv_dtype, float k_scale,
-                         float v_scale, const int32_t *block_table, int block_table_stride,
-                         int num_blocks, int page_size, const int32_t *seq_lens,
-                         const int32_t *cu_seqlens_q, const int32_t *plan, int plan_capacity,
-                         int bs, int num_tokens, int max_q_len, int num_q_heads, int num_kv_heads,
-                         int head_dim, float sm_scale, int causal, int num_sms, int seg_max,
-                         float *part_o, float *part_m, float *part_l, void *stream)
+}  // extern "C"
+
+namespace sk {
+
+// Checks the arguments of an attention call and resolves the kernel's parameters; launches
+// nothing.  *rp_out is the row tile of the launch, 0 when there is nothing to launch.
+int prepare_attn(const void *q, const void *kv_pages, int kv_dtype, float k_scale, float v_scale,
+                 const int32_t *block_table, int block_table_stride, int num_blocks, int page_size,
+                 const int32_t *seq_lens, const int32_t *cu_seqlens_q, const int32_t *plan,
+                 int plan_capacity, int bs, int num_tokens, int max_q_len, int num_q_heads,
+                 int num_kv_heads, int head_dim, float sm_scale, int causal, int num_sms, int seg_max,
+                 float *part_o, float *part_m, float *part_l, AttnParams *params, int *rp_out)
 {
     if (q == nullptr || kv_pages == nullptr || block_table == nullptr || seq_lens == nullptr ||
         cu_seqlens_q == nullptr || part_o == nullptr || part_m == nullptr || part_l == nullptr)
@@ -257,10 +295,9 @@ int sk_paged_decode_attn(const void *q, const void *kv_pages, int kv_dtype, floa
     int num_items;
     int fixed = 0;
     if (plan != nullptr) {
-        const int budget = num_sms / num_kv_heads;
-        const int need = 1 + (budget > bs ? budget : bs);
+        const long long need = capacity_of(bs, num_kv_heads, num_sms);
         if (plan_capacity < need)
-            return fail(SK_ERR_CAPACITY, "sk_paged_decode_attn: plan_capacity=%d < %d", plan_capacity,
+            return fail(SK_ERR_CAPACITY, "sk_paged_decode_attn: plan_capacity=%d < %lld", plan_capacity,
                         need);
         num_items = plan_capacity - 1;
     } else {
@@ -278,6 +315,7 @@ int sk_paged_decode_attn(const void *q, const void *kv_pages, int kv_dtype, floa
     const int row_blocks = rp > 0 ? (rows_max + rp - 1) / rp : 1;
     if ((long long)num_items * num_kv_heads * row_blocks > 0x7FFFFFFFLL)
         return fail(SK_ERR_INVALID, "sk_paged_decode_attn: grid too large");
+    *rp_out = 0;
     if (num_tokens == 0)
         return SK_OK;
 
@@ -286,7 +324,7 @@ int sk_paged_decode_attn(const void *q, const void *kv_pages, int kv_dtype, floa
     if (rc != SK_OK)
         return rc;
 
-    AttnParams p;
+    AttnParams &p = *params;
     p.q = static_cast<const uint16_t *>(q);
     p.kv = kv_pages;
     p.block_table = block_table;
@@ -312,17 +350,16 @@ int sk_paged_decode_attn(const void *q, const void *kv_pages, int kv_dtype, floa
     const float log2e = 1.4426950408889634f;
     p.score_scale_log2 = sm_scale * (kv_dtype == SK_KV_FP8_E4M3 ? k_scale : 1.f) * log2e;
     p.v_scale = kv_dtype == SK_KV_FP8_E4M3 ? v_scale : 1.f;
+    p.wait_limit = wait_limit();
 
     p.row_blocks = row_blocks;
-    cudaError_t e = launch_attn_tc(p, kv_dtype, rp, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess)
-        return cuda_fail(e, "attention kernel launch");
+    *rp_out = rp;
     return SK_OK;
 }
 
-int sk_merge_segments(const float *part_o, const float *part_m, const float *part_l,
-                      const int32_t *tok_nseg, int fixed_nseg, int num_tokens, int num_q_heads,
-                      int head_dim, int seg_max, void *out, float *lse, void *stream)
+// Checks the arguments of a merge call; launches nothing.
+int check_merge(const float *part_o, const float *part_m, const float *part_l, const int32_t *tok_nseg,
+                int fixed_nseg, int num_tokens, int num_q_heads, int head_dim, int seg_max, const void *out)
 {
     if (part_o == nullptr || part_m == nullptr || part_l == nullptr || out == nullptr)
         return fail(SK_ERR_INVALID, "sk_merge_segments: null pointer argument");
@@ -335,6 +372,48 @@ int sk_merge_segments(const float *part_o, const float *part_m, const float *par
         return fail(SK_ERR_INVALID, "sk_merge_segments: fixed_nseg=%d outside [0, seg_max]", fixed_nseg);
     if ((reinterpret_cast<uintptr_t>(part_o) & 15) || (reinterpret_cast<uintptr_t>(out) & 7))
         return fail(SK_ERR_INVALID, "sk_merge_segments: part_o must be 16-byte and out 8-byte aligned");
+    return SK_OK;
+}
+
+int launch_prepared_attn(const AttnParams &p, int kv_dtype, int rp, void *stream)
+{
+    cudaError_t e = launch_attn_tc(p, kv_dtype, rp, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "attention kernel launch");
+    return SK_OK;
+}
+
+}  // namespace sk
+
+extern "C" {
+
+int sk_paged_decode_attn(const void *q, const void *kv_pages, int kv_dtype, float k_scale,
+                         float v_scale, const int32_t *block_table, int block_table_stride,
+                         int num_blocks, int page_size, const int32_t *seq_lens,
+                         const int32_t *cu_seqlens_q, const int32_t *plan, int plan_capacity,
+                         int bs, int num_tokens, int max_q_len, int num_q_heads, int num_kv_heads,
+                         int head_dim, float sm_scale, int causal, int num_sms, int seg_max,
+                         float *part_o, float *part_m, float *part_l, void *stream)
+{
+    AttnParams p;
+    int rp = 0;
+    const int rc = prepare_attn(q, kv_pages, kv_dtype, k_scale, v_scale, block_table, block_table_stride,
+                                num_blocks, page_size, seq_lens, cu_seqlens_q, plan, plan_capacity, bs,
+                                num_tokens, max_q_len, num_q_heads, num_kv_heads, head_dim, sm_scale,
+                                causal, num_sms, seg_max, part_o, part_m, part_l, &p, &rp);
+    if (rc != SK_OK || rp == 0)
+        return rc;
+    return launch_prepared_attn(p, kv_dtype, rp, stream);
+}
+
+int sk_merge_segments(const float *part_o, const float *part_m, const float *part_l,
+                      const int32_t *tok_nseg, int fixed_nseg, int num_tokens, int num_q_heads,
+                      int head_dim, int seg_max, void *out, float *lse, void *stream)
+{
+    const int rc = check_merge(part_o, part_m, part_l, tok_nseg, fixed_nseg, num_tokens, num_q_heads,
+                               head_dim, seg_max, out);
+    if (rc != SK_OK)
+        return rc;
     cudaError_t e = launch_merge(part_o, part_m, part_l, tok_nseg, fixed_nseg, num_tokens, num_q_heads,
                                  seg_max, static_cast<uint16_t *>(out), lse,
                                  static_cast<cudaStream_t>(stream));
@@ -431,6 +510,9 @@ int sk_get_device_status(void *stream, int clear)
         e = cudaStreamSynchronize(st);
     if (e != cudaSuccess)
         return cuda_fail(e, "reading the device status word");
+    g_last_device_status = value;
+    if (value & SK_DEV_TIMEOUT)
+        return fail(SK_ERR_TIMEOUT, "a bounded wait inside a kernel expired (device status 0x%x)", value);
     return value;
 }
 

@@ -49,9 +49,12 @@
 // 2R columns of P^T, so O^T holds O_hi | O_lo, added at the end.  The scales
 // k_scale and v_scale are folded into the score scale and the output.
 //
-// Every mbarrier wait is bounded (about two seconds); on expiry the CTA sets
-// SK_DEV_TIMEOUT in the device status word, waits (bounded) for its own copies
-// and MMAs in flight, frees TMEM and exits.
+// Every mbarrier wait is bounded (about two seconds unless sk_set_wait_limit
+// says otherwise); on expiry the CTA sets SK_DEV_TIMEOUT in the device status
+// word and every role gives up.  Before the CTA exits, the producer waits for
+// every copy it issued to land and each issuer for its last commit (these waits
+// keep the two-second bound whatever the limit), so no copy or product outlives
+// the CTA's shared memory or TMEM.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
@@ -69,7 +72,7 @@ using namespace sm100;
 
 constexpr int kTokTile = 128;                       // tokens per MMA (M)
 constexpr int kSoftmaxWarp0 = 2;
-constexpr long long kWaitLimit = 4000000000LL;      // cycles (~2 s)
+constexpr long long kDrainLimit = 4000000000LL;     // cycles (~2 s): waits for work already issued
 constexpr uint32_t kFull = 0xffffffffu;
 constexpr int kMaxSmem = 232448;                    // 227 KB per CTA
 
@@ -248,6 +251,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
     extern __shared__ __align__(1024) uint8_t smem[];
 
     wait_prior_grid();    // the plan, Q and the pages may come from the kernels before this one
+    // the fixed split has no plan kernel to check that cu_seqlens_q covers [0, num_tokens)
+    if (p.plan == nullptr && blockIdx.x == 0 && threadIdx.x == 0 &&
+        (__ldg(p.cu_q) != 0 || __ldg(p.cu_q + p.bs) != p.num_tokens))
+        atomicOr(p.status, SK_DEV_BAD_SEQ);
     // CTA b: row block b % row_blocks (neighbouring CTAs share a work item's pages, so
     // the later reads of a page find it in L2) of work item / KV head b / row_blocks.
     const int ih = blockIdx.x / p.row_blocks;
@@ -448,7 +455,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
         for (int j = 0; j < ntiles && ok; ++j) {
             const int st = j % C::kStages;
             if (j >= C::kStages)
-                ok = mbar_wait_bounded(bar_empty(st), ((j / C::kStages) - 1) & 1, abort_flag, kWaitLimit);
+                ok = mbar_wait_bounded(bar_empty(st), ((j / C::kStages) - 1) & 1, abort_flag, p.wait_limit);
             ok = __all_sync(kFull, ok);
             if (!ok)
                 break;
@@ -488,10 +495,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             *abort_flag = 1;
             if (lane == 0)
                 atomicOr(p.status, SK_DEV_TIMEOUT);
-            // let every copy already issued land before the CTA exits
-            for (int t = issued > C::kStages ? issued - C::kStages : 0; t < issued; ++t)
-                mbar_wait_bounded(bar_full(t % C::kStages), (t / C::kStages) & 1, nullptr, kWaitLimit);
         }
+        // Every copy issued lands before the CTA exits, even when a consumer gave up before
+        // waiting for it.  Tiles before issued - kStages were consumed before their stage was
+        // reused; each of the last kStages tiles is the last phase its barrier will see, so these
+        // waits are unambiguous and return at once when the consumers already saw them land.
+        for (int t = issued > C::kStages ? issued - C::kStages : 0; t < issued; ++t)
+            mbar_wait_bounded(bar_full(t % C::kStages), (t / C::kStages) & 1, nullptr, kDrainLimit);
     } else if (warp == 1 || warp == C::kPvWarp) {
         // ================================================================ MMA issuers
         // Whole warps run these loops; one elected lane issues each MMA and commit.
@@ -521,11 +531,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             for (int j = 0; j < ntiles && ok; ++j) {
                 const int st = j % C::kStages, b = j % C::kSBufs;
                 if (j >= C::kSBufs)
-                    ok = mbar_wait_bounded(bar_sfree(b), ((j / C::kSBufs) - 1) & 1, abort_flag, kWaitLimit);
+                    ok = mbar_wait_bounded(bar_sfree(b), ((j / C::kSBufs) - 1) & 1, abort_flag, p.wait_limit);
                 if (ok && j >= C::kSBufs)     // PV(j - kSBufs) issued: phase j / kSBufs - 1 of pvis[b]
-                    ok = mbar_wait_bounded(bar_pvis(b), ((j / C::kSBufs) - 1) & 1, abort_flag, kWaitLimit);
+                    ok = mbar_wait_bounded(bar_pvis(b), ((j / C::kSBufs) - 1) & 1, abort_flag, p.wait_limit);
                 if (ok)
-                    ok = mbar_wait_bounded(bar_full(st), (j / C::kStages) & 1, abort_flag, kWaitLimit);
+                    ok = mbar_wait_bounded(bar_full(st), (j / C::kStages) & 1, abort_flag, p.wait_limit);
                 ok = __all_sync(kFull, ok);
                 if (!ok)
                     break;
@@ -563,14 +573,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                     *abort_flag = 1;
                     atomicOr(p.status, SK_DEV_TIMEOUT);
                 }
-                if (last >= 0)     // let this warp's MMAs finish before TMEM is freed
-                    mbar_wait_bounded(bar_sfull(last % C::kSBufs), (last / C::kSBufs) & 1, nullptr, kWaitLimit);
             }
+            // this warp's products finish before TMEM is freed, also when the softmax gave up
+            // before consuming them (QK(last) is the last commit sfull[last % kSBufs] sees)
+            if (last >= 0)
+                mbar_wait_bounded(bar_sfull(last % C::kSBufs), (last / C::kSBufs) & 1, nullptr, kDrainLimit);
         } else {
             // PV(i) as soon as the softmax threads have written P(i).  Its completion frees the
             // stage (empty), which is also how the softmax learns that O holds tile i.
             for (int i = 0; i < ntiles && ok; ++i) {
-                ok = mbar_wait_bounded(bar_pfull(i % C::kSBufs), (i / C::kSBufs) & 1, abort_flag, kWaitLimit);
+                ok = mbar_wait_bounded(bar_pfull(i % C::kSBufs), (i / C::kSBufs) & 1, abort_flag, p.wait_limit);
                 ok = __all_sync(kFull, ok);
                 if (!ok)
                     break;
@@ -600,9 +612,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                     *abort_flag = 1;
                     atomicOr(p.status, SK_DEV_TIMEOUT);
                 }
-                if (last >= 0)
-                    mbar_wait_bounded(bar_odone, 0, nullptr, kWaitLimit);
             }
+            // every PV completes before TMEM is freed, also when the softmax gave up waiting
+            if (last >= 0)
+                mbar_wait_bounded(bar_odone, 0, nullptr, kDrainLimit);
         }
         __syncwarp();
     } else {
@@ -634,7 +647,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             const int st = j % C::kStages;
             constexpr int NH = C::kHalves;
             float x[NH][RH];                    // this thread's tokens: tau, 128 + tau
-            bool ok = !failed && mbar_wait_bounded(bar_sfull(sb), (j / C::kSBufs) & 1, abort_flag, kWaitLimit);
+            bool ok = !failed && mbar_wait_bounded(bar_sfull(sb), (j / C::kSBufs) & 1, abort_flag, p.wait_limit);
             ok = __all_sync(kFull, ok);          // tcgen05.ld is warp-collective
             if (ok) {
                 tc_fence_after();
@@ -741,7 +754,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                     // PV(j-1-kStages), was seen by the producer before it loaded tile j-1, and the one
                     // after, PV(j-1+kStages), cannot start before P(j+1): PV(j-1)'s is unambiguous here.
                     const int jp = j - 1;
-                    bool okp = mbar_wait_bounded(bar_empty(jp % C::kStages), (jp / C::kStages) & 1, abort_flag, kWaitLimit);
+                    bool okp = mbar_wait_bounded(bar_empty(jp % C::kStages), (jp / C::kStages) & 1, abort_flag, p.wait_limit);
                     okp = __all_sync(kFull, okp);    // tcgen05.ld/st are warp-collective
                     if (okp) {
                         tc_fence_after();
@@ -883,7 +896,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             alpha_s[r0 + tid] = (gred[tid] + gred[32 + tid]) + (gred[64 + tid] + gred[96 + tid]);
         bool okf = !failed;
         if (okf && ntiles > 0)
-            okf = mbar_wait_bounded(bar_odone, 0, abort_flag, kWaitLimit);
+            okf = mbar_wait_bounded(bar_odone, 0, abort_flag, p.wait_limit);
         // the group's verdict; the barrier also publishes the row sums written above
         const bool write = !named_bar_or(bar_id, 128, !okf);
         if (write) {

@@ -33,6 +33,7 @@ struct AttnParams {
     int causal;
     float score_scale_log2;      // sm_scale * k_scale * log2(e)
     float v_scale;               // applied to o (1 for bf16)
+    long long wait_limit;        // clock cycles an abortable mbarrier wait may take (sk_set_wait_limit)
 };
 
 // A decoded work item.
@@ -127,8 +128,26 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 
 // Address of the current device's status word (looked up once per device).
 int device_status_word(int **out);
+// Default limit of the attention kernel's abortable waits: about two seconds of SM clock.
+constexpr long long kDefaultWaitLimit = 4000000000LL;
+// The limit in force (sk_set_wait_limit).
+long long wait_limit();
 // Records `msg` as this thread's last error and returns `code`.
 int set_error(int code, const char *msg);
+
+// Host halves of sk_paged_decode_attn and sk_merge_segments, so that a composite call can check
+// every argument before it launches anything.  prepare_attn validates and resolves the kernel
+// parameters (*rp_out = 0: nothing to launch); launch_prepared_attn launches them; check_merge
+// validates a merge call.  All return an sk_status.
+int prepare_attn(const void *q, const void *kv_pages, int kv_dtype, float k_scale, float v_scale,
+                 const int32_t *block_table, int block_table_stride, int num_blocks, int page_size,
+                 const int32_t *seq_lens, const int32_t *cu_seqlens_q, const int32_t *plan,
+                 int plan_capacity, int bs, int num_tokens, int max_q_len, int num_q_heads,
+                 int num_kv_heads, int head_dim, float sm_scale, int causal, int num_sms, int seg_max,
+                 float *part_o, float *part_m, float *part_l, AttnParams *params, int *rp_out);
+int launch_prepared_attn(const AttnParams &p, int kv_dtype, int rp, void *stream);
+int check_merge(const float *part_o, const float *part_m, const float *part_l, const int32_t *tok_nseg,
+                int fixed_nseg, int num_tokens, int num_q_heads, int head_dim, int seg_max, const void *out);
 
 // Launchers (each returns a cudaError_t from the launch).
 cudaError_t launch_plan(const int32_t *seq_lens, const int32_t *cu_q, int bs, int num_tokens,

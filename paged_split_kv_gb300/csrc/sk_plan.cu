@@ -225,6 +225,19 @@ plan_kernel(const int32_t *__restrict__ seq_lens, const int32_t *__restrict__ cu
     }
     if (1 + total_items > plan_capacity && tid == 0)
         atomicOr(status, SK_DEV_BAD_SEQ);
+    // cu_seqlens_q must cover [0, num_tokens) exactly: cu[0] == 0 and cu[bs] == num_tokens.  Tokens
+    // outside [cu[0], cu[bs]) belong to no sequence; they get 0 segments (the merge writes 0 for
+    // them), and the status word reports the inconsistency.
+    {
+        const int first = __ldg(cu_q), last = __ldg(cu_q + bs);
+        if (tid == 0 && (first != 0 || last != num_tokens))
+            atomicOr(status, SK_DEV_BAD_SEQ);
+        const int lo_end = min(max(first, 0), num_tokens), hi_begin = min(max(last, 0), num_tokens);
+        for (int t = tid; t < lo_end; t += nthr)
+            tok_nseg[t] = 0;
+        for (int t = max(hi_begin, lo_end) + tid; t < num_tokens; t += nthr)
+            tok_nseg[t] = 0;
+    }
     for (long long k = 1 + total_items + tid; k < plan_capacity; k += nthr)
         plan[k] = -1;
 }

@@ -50,17 +50,38 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+// Non-blocking test of the same condition: returns at once.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Limits below this many cycles poll with test_wait instead of suspending in
+// try_wait: a try_wait may suspend for a hardware-chosen time longer than the
+// limit (long enough to cover a copy's whole memory latency), so only polling
+// lets a very short limit expire.
+constexpr long long kPollBelowCycles = 100000;
+
 // Waits for the phase with the given parity to complete.  Gives up after
 // `limit` clock cycles, or when `abort` is not null and *abort becomes
 // nonzero; returns false then.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, const volatile int *abort,
                                                   long long limit)
 {
-    if (mbar_try_wait(bar, parity))
+    const bool poll = limit < kPollBelowCycles;
+    if (poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity))
         return true;
     const long long t0 = clock64();
     while (true) {
-        if (mbar_try_wait(bar, parity))
+        if (poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity))
             return true;
         if (abort != nullptr && *abort)
             return false;

@@ -43,6 +43,11 @@ std::mutex g_scratch_mutex;
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+const char *const kCapacityMsg =
+    "sk_paged_decode_attention_static: the call needs more scratch than the 32 MiB static array "
+    "(num_tokens * seg_max * num_q_heads * (head_dim + 2) * 4 bytes plus the plan); lower seg_max "
+    "or split the batch";
+
 // Device address of g_static_scratch on the current device.  In host code the
 // array's name is only a host-side stand-in, never a device pointer.
 int scratch_address(unsigned char **out)
@@ -86,9 +91,16 @@ extern "C" int sk_paged_decode_attention_static(
         return set_error(SK_ERR_INVALID, "sk_paged_decode_attention_static: bad sizes");
 
     // scratch layout: plan | tok_nseg | part_m | part_l | part_o, each 256-byte aligned
-    const int budget = num_sms / num_kv_heads;
-    const int capacity = 1 + (budget > bs ? budget : bs);
-    const size_t rows = (size_t)num_tokens * (size_t)seg_max * (size_t)num_q_heads;
+    const int capacity = sk_plan_capacity(bs, num_kv_heads, num_sms);
+    if (capacity < 0)
+        return capacity;
+    // rows = num_tokens * seg_max * num_q_heads, each (head_dim + 2) * 4 bytes of partials; the
+    // bound is checked by division first, so none of the products below can wrap
+    const size_t per_row = (size_t)(head_dim + 2) * 4;
+    const size_t heads_segs = (size_t)seg_max * (size_t)num_q_heads;    // < 2^47
+    if (num_tokens > 0 && heads_segs > kStaticScratchBytes / per_row / (size_t)num_tokens)
+        return set_error(SK_ERR_CAPACITY, kCapacityMsg);
+    const size_t rows = (size_t)num_tokens * heads_segs;
     const size_t off_plan = 0;
     const size_t off_tok = align256(off_plan + (use_plan ? (size_t)capacity * 4 : 0));
     const size_t off_m = align256(off_tok + (use_plan ? (size_t)num_tokens * 4 : 0));
@@ -96,10 +108,7 @@ extern "C" int sk_paged_decode_attention_static(
     const size_t off_o = align256(off_l + rows * 4);
     const size_t need = off_o + rows * (size_t)head_dim * 4;
     if (need > kStaticScratchBytes)
-        return set_error(SK_ERR_CAPACITY,
-                         "sk_paged_decode_attention_static: the call needs more scratch than the "
-                         "32 MiB static array (num_tokens * seg_max * num_q_heads * (head_dim + 2) * 4 "
-                         "bytes plus the plan); lower seg_max or split the batch");
+        return set_error(SK_ERR_CAPACITY, kCapacityMsg);
 
     unsigned char *base = nullptr;
     int rc = scratch_address(&base);
@@ -112,26 +121,39 @@ extern "C" int sk_paged_decode_attention_static(
     float *part_o = reinterpret_cast<float *>(base + off_o);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
+    // every argument is checked before the first launch
+    if (use_plan && (seq_lens == nullptr || cu_seqlens_q == nullptr))
+        return set_error(SK_ERR_INVALID, "sk_paged_decode_attention_static: null seq_lens or cu_seqlens_q");
+    AttnParams params;
+    int rp = 0;
+    rc = prepare_attn(q, kv_pages, kv_dtype, k_scale, v_scale, block_table, block_table_stride, num_blocks,
+                      page_size, seq_lens, cu_seqlens_q, plan, capacity, bs, num_tokens, max_q_len, num_q_heads,
+                      num_kv_heads, head_dim, sm_scale, causal, num_sms, seg_max, part_o, part_m, part_l, &params,
+                      &rp);
+    if (rc != SK_OK)
+        return rc;
+    const int fixed = use_plan ? 0 : sk_fixed_nseg(bs, num_kv_heads, num_sms, seg_max);
+    rc = check_merge(part_o, part_m, part_l, tok, fixed, num_tokens, num_q_heads, head_dim, seg_max, out);
+    if (rc != SK_OK)
+        return rc;
+
     if (use_plan) {
-        if (seq_lens == nullptr || cu_seqlens_q == nullptr)
-            return set_error(SK_ERR_INVALID, "sk_paged_decode_attention_static: null seq_lens or cu_seqlens_q");
         int *status = nullptr;
         rc = device_status_word(&status);
         if (rc != SK_OK)
             return rc;
         // built on every call: the caller's lengths may have changed in place
+        const int budget = num_sms / num_kv_heads;   // B of the plan rule
         cudaError_t e = launch_plan(seq_lens, cu_seqlens_q, bs, num_tokens, budget, seg_max, plan,
                                     capacity, tok, status, st);
         if (e != cudaSuccess)
             return set_error(SK_ERR_CUDA, "sk_paged_decode_attention_static: plan kernel launch failed");
     }
-    rc = sk_paged_decode_attn(q, kv_pages, kv_dtype, k_scale, v_scale, block_table, block_table_stride,
-                              num_blocks, page_size, seq_lens, cu_seqlens_q, plan, capacity, bs,
-                              num_tokens, max_q_len, num_q_heads, num_kv_heads, head_dim, sm_scale,
-                              causal, num_sms, seg_max, part_o, part_m, part_l, stream);
-    if (rc < 0)
-        return rc;
-    const int fixed = use_plan ? 0 : sk_fixed_nseg(bs, num_kv_heads, num_sms, seg_max);
+    if (rp > 0) {
+        rc = launch_prepared_attn(params, kv_dtype, rp, stream);
+        if (rc != SK_OK)
+            return rc;
+    }
     return sk_merge_segments(part_o, part_m, part_l, tok, fixed, num_tokens, num_q_heads, head_dim,
                              seg_max, out, lse, stream);
 }

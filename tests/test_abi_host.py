@@ -138,3 +138,107 @@ def test_python_binding_refuses_cpu_tensors(sklib):
     with pytest.raises(ValueError):
         sk.sk_build_plan(torch.zeros(2, dtype=torch.int32), torch.zeros(3, dtype=torch.int32), 1,
                          torch.zeros(10, dtype=torch.int32), torch.zeros(2, dtype=torch.int32), 148)
+
+
+def test_plan_capacity_is_computed_by_the_library(sklib, oracle):
+    import paged_split_kv_gb300 as sk
+    for bs in (1, 2, 16, 73, 74, 75, 128, 32767):
+        for kv in (1, 2, 8):
+            for nsm in (148, 152, 256):
+                assert sklib.sk_plan_capacity(bs, kv, nsm) == 1 + max(nsm // kv, bs)
+                assert sk.plan_capacity(bs, kv, nsm) == sklib.sk_plan_capacity(bs, kv, nsm)
+    assert sklib.sk_plan_capacity(0, 2, 148) == -1
+    assert sklib.sk_plan_capacity(40000, 2, 148) == -1
+    assert sklib.sk_plan_capacity(4, 0, 148) == -1
+
+
+def test_wait_limit_round_trip(sklib):
+    default = sklib.sk_set_wait_limit(-1)
+    assert default == 4000000000
+    assert sklib.sk_set_wait_limit(0) == default
+    assert sklib.sk_set_wait_limit(-1) == 0
+    assert sklib.sk_set_wait_limit(-1) == default
+
+
+def test_static_entry_rejects_sizes_that_would_wrap(sklib):
+    """The scratch size of the allocation-free call is bounded by division, so a
+    head count that would wrap the byte count is a capacity error, not a small
+    size (checked before any CUDA call)."""
+    f = sklib.sk_paged_decode_attention_static
+
+    def call(nt=4, hq=32, hkv=2, seg=64, bs=1):
+        return f(FAKE, FAKE, 0, 1.0, 1.0, FAKE, 10, 100, 16, FAKE, FAKE, 1, bs, nt, 4, hq, hkv, 128,
+                 0.088, 1, 148, seg, FAKE, None, None)
+    assert call(nt=1 << 20) == -2
+    assert call(nt=0x7FFFFFFF, hq=0x40000000, hkv=1, seg=0xFFFF) == -2
+    assert call(nt=2, hq=0x7FFFFFFE, hkv=1, seg=0xFFFF) == -2
+    assert b"32 MiB" in sklib.sk_last_error()
+    assert call(hq=0) == -1
+
+
+def _cpu_batch(torch, nt=8, hq=8, hkv=2, d=128, bs=2, nb=4, stride=3, seg=4):
+    return dict(q=torch.zeros((nt, hq, d), dtype=torch.bfloat16),
+                kv=torch.zeros((nb, hkv, 16, 2 * d), dtype=torch.bfloat16),
+                bt=torch.zeros((bs, stride), dtype=torch.int32),
+                lens=torch.zeros(bs, dtype=torch.int32), cu=torch.zeros(bs + 1, dtype=torch.int32),
+                po=torch.zeros((nt, seg, hq, d)), pm=torch.zeros((nt, seg, hq)), pl=torch.zeros((nt, seg, hq)),
+                out=torch.zeros((nt, hq, d), dtype=torch.bfloat16), lse=torch.zeros((nt, hq)),
+                tok=torch.zeros(nt, dtype=torch.int32))
+
+
+def test_python_binding_checks_shapes_before_raw_pointers(sklib):
+    """Every wrapper rejects a tensor whose shape would make a kernel read or write
+    past it, before anything reaches the library (here on CPU tensors: the shape
+    check comes before the device check)."""
+    import torch
+    import paged_split_kv_gb300 as sk
+
+    def attn(b):
+        return sk.sk_paged_decode_attn(b["q"], b["kv"], b["bt"], b["lens"], b["cu"], None, b["po"], b["pm"],
+                                       b["pl"], max_q_len=4, sm_scale=0.1, num_sms=148)
+
+    def static(b):
+        return sk.sk_paged_decode_attention_static(b["q"], b["kv"], b["bt"], b["lens"], b["cu"], b["out"],
+                                                   b["lse"], max_q_len=4, sm_scale=0.1, num_sms=148)
+
+    def merge(b):
+        return sk.sk_merge_segments(b["po"], b["pm"], b["pl"], b["tok"], b["out"], b["lse"])
+
+    bad = {
+        "kv last dim": dict(kv=torch.zeros((4, 2, 16, 128), dtype=torch.bfloat16)),
+        "cu entries": dict(cu=torch.zeros(4, dtype=torch.int32)),
+        "block-table rows": dict(bt=torch.zeros((1, 3), dtype=torch.int32)),
+        "head ratio": dict(kv=torch.zeros((4, 3, 16, 256), dtype=torch.bfloat16)),
+    }
+    for name, kw in bad.items():
+        for fn in (attn, static):
+            b = _cpu_batch(torch)
+            b.update(kw)
+            with pytest.raises(ValueError):
+                fn(b)
+    for name, kw in {"part_o": dict(po=torch.zeros((8, 4, 8, 64))), "part_m": dict(pm=torch.zeros((8, 3, 8))),
+                     "part_l": dict(pl=torch.zeros((7, 4, 8)))}.items():
+        b = _cpu_batch(torch)
+        b.update(kw)
+        with pytest.raises(ValueError, match=name):
+            attn(b)
+    for name, kw in {"out": dict(out=torch.zeros((8, 8, 64), dtype=torch.bfloat16)),
+                     "lse": dict(lse=torch.zeros((8, 4))), "tok_nseg": dict(tok=torch.zeros(9, dtype=torch.int32)),
+                     "part_m": dict(pm=torch.zeros((8, 4, 4)))}.items():
+        b = _cpu_batch(torch)
+        b.update(kw)
+        with pytest.raises(ValueError, match=name):
+            merge(b)
+    for name, kw in {"out": dict(out=torch.zeros((7, 8, 128), dtype=torch.bfloat16)),
+                     "lse": dict(lse=torch.zeros((8, 9)))}.items():
+        b = _cpu_batch(torch)
+        b.update(kw)
+        with pytest.raises(ValueError, match=name):
+            static(b)
+    with pytest.raises(ValueError, match="cu_seqlens_q"):
+        sk.sk_build_plan(torch.zeros(2, dtype=torch.int32), torch.zeros(2, dtype=torch.int32), 1,
+                         torch.zeros(10, dtype=torch.int32), torch.zeros(2, dtype=torch.int32), 148)
+    # well-shaped CPU tensors get as far as the device check
+    for fn in (attn, static, merge):
+        with pytest.raises(ValueError, match="CUDA"):
+            fn(_cpu_batch(torch))
