@@ -15,7 +15,12 @@ Metric: effective KV-read TB/s = K/V bytes of the batch / time per step
 
 Besides the contract's keys the line carries e2e_serving: the same step as a
 server runs it (cache resident in HBM, the step's new K/V written by
-sk_reshape_and_cache, inputs copied from pinned host memory, one CUDA graph).
+sk_reshape_and_cache, inputs copied from pinned host memory, one CUDA graph);
+per_config: every other workload (1 and 3-8) timed the same way on the same
+box, one at a time, with its per-kernel split, KV TB/s, roofline fraction and
+clocks (no CPU or e2e legs; --no-per-config skips them); and skew_vs_uniform:
+the agentic batch's KV TB/s over the uniform batch's, for attention + merge and
+for the whole step.
 Other modes print a line of their own:
 
   python bench.py --config I --forward-layers 15   # one plan + 15 layers, CUDA graph
@@ -59,7 +64,7 @@ def _args():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="sk", choices=["sk", "reference"])
-    ap.add_argument("--config", type=int, default=2, help="workload 1..7 (default 2)")
+    ap.add_argument("--config", type=int, default=2, help="workload 1..8 (default 2)")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -72,6 +77,8 @@ def _args():
                     help="time the KV write step (65536 tokens x 8 KV heads) instead of the path")
     ap.add_argument("--eager", action="store_true",
                     help="launch every step from Python instead of replaying the steps as one CUDA graph")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the other workloads' per_config summaries in the default line")
     ap.add_argument("--fixed-split", action="store_true",
                     help="time the fixed split even when bs > 1 (bs == 1 always uses it, as the method does)")
     return ap.parse_args()
@@ -345,6 +352,218 @@ def _ncu_traffic(workload, sha):
 
 # ----------------------------------------------------------------------------- GPU arm
 
+class PathBench:
+    """Device buffers of one workload and the timed replay of its steps.
+
+    One step = plan-cache reset, plan (unless the fixed split runs), attention,
+    merge.  The timed steps (and the warm-up) are captured once as a CUDA graph
+    (every call is capture safe) and replayed once: the device runs exactly the
+    kernels of K eager steps, but the timing does not depend on how fast the
+    host issues the calls.  Inputs larger than L2 run the K steps back to back
+    between one event pair (an event between two steps would cut the overlap of
+    one step's last kernel with the next step's first launch, ~5 us per step);
+    smaller inputs get an L2 flush before every step and an event pair around
+    each step, so the flushes stay out of the sum.  A second graph of the same
+    steps, with events around each kernel, gives the per-kernel split.
+    ``eager`` keeps Python-launched loops instead."""
+
+    def __init__(self, sk, torch, w, dev, fixed_split=False, eager=False):
+        self.sk, self.torch, self.w, self.dev = sk, torch, w, dev
+        self.use_plan = w.bs > 1 and not fixed_split
+        nt, hq, d = w.num_tokens, w.num_q_heads, w.head_dim
+        self.q = si.make_q(w, dev)
+        self.kv = si.make_kv(w, dev)
+        self.bt = torch.as_tensor(w.block_table, device=dev)
+        self.lens = torch.as_tensor(w.seq_lens, device=dev)
+        self.cu = torch.as_tensor(w.cu_q, device=dev)
+        cap = sk.plan_capacity(w.bs, w.num_kv_heads, w.num_sms)
+        self.plan = torch.empty(cap, dtype=torch.int32, device=dev) if self.use_plan else None
+        self.tok = torch.empty(nt, dtype=torch.int32, device=dev) if self.use_plan else None
+        self.part_o = torch.empty((nt, w.seg_max, hq, d), dtype=torch.float32, device=dev)
+        self.part_m = torch.empty((nt, w.seg_max, hq), dtype=torch.float32, device=dev)
+        self.part_l = torch.empty((nt, w.seg_max, hq), dtype=torch.float32, device=dev)
+        self.out = torch.empty((nt, hq, d), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((nt, hq), dtype=torch.float32, device=dev)
+        self.fixed = 0 if self.use_plan else sk.sk_fixed_nseg(w.bs, w.num_kv_heads, w.num_sms, w.seg_max)
+        # L2 flush for inputs that fit in L2: a write larger than L2, then a read of another buffer
+        # larger than L2, which evicts the written (dirty) lines, so that their write-backs to HBM
+        # happen in the flush and not inside the timed step
+        small = w.kv_bytes <= 129e6
+        self.flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if small else None
+        self.flush_rd = torch.ones(256 << 20, dtype=torch.uint8, device=dev) if small else None
+        self.flush_sink = torch.zeros(1, dtype=torch.int64, device=dev) if small else None
+        try:
+            self.graphs = not eager and torch.cuda.Event(enable_timing=True, external=True) is not None
+        except TypeError:                  # a PyTorch without graph-recorded events
+            self.graphs = False
+        self.stream = torch.cuda.Stream(device=dev) if self.graphs else torch.cuda.current_stream()
+
+    def step(self, ev=None):
+        # ev: None, [start, end] of the step, or [start, after plan, after attention, end].  Events
+        # between kernels cut the launch overlap of dependent kernels, so the timed steps carry the
+        # pair only and a second replay of the same steps gives the per-kernel split.
+        sk, w, st = self.sk, self.w, self.stream
+        parts = ev is not None and len(ev) == 4
+        if self.flush is not None:
+            self.flush.fill_(1)
+            self.torch.sum(self.flush_rd.view(self.torch.int64), dim=0, keepdim=True, out=self.flush_sink)
+        if ev is not None and ev[0] is not None:
+            ev[0].record(st)
+        if self.use_plan:
+            sk.sk_plan_cache_reset()
+            sk.sk_build_plan(self.lens, self.cu, w.num_kv_heads, self.plan, self.tok, w.num_sms, w.seg_max, st)
+        if parts:
+            ev[1].record(st)
+        sk.sk_paged_decode_attn(self.q, self.kv, self.bt, self.lens, self.cu, self.plan, self.part_o,
+                                self.part_m, self.part_l, max_q_len=w.max_q_len, sm_scale=w.sm_scale,
+                                num_sms=w.num_sms, k_scale=w.k_scale, v_scale=w.v_scale,
+                                causal=bool(w.causal), stream=st)
+        if parts:
+            ev[2].record(st)
+        sk.sk_merge_segments(self.part_o, self.part_m, self.part_l, self.tok, self.out, self.lse,
+                             fixed_nseg=self.fixed, stream=st)
+        if ev is not None and ev[-1] is not None:
+            ev[-1].record(st)
+
+    def run(self, steps, warmup, ws=1, sampler=None):
+        """Warm-up, K timed steps, then K steps with events around each kernel.  Returns
+        {local_ms, plan_ms, attn_ms, merge_ms, clocks}."""
+        torch = self.torch
+        flushed = self.flush is not None
+        if sampler:
+            sampler.start()
+        self.stream.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(self.stream):
+            for _ in range(3):
+                self.step()
+        torch.cuda.synchronize()
+        ext = {"external": True} if self.graphs else {}
+        evs = [[torch.cuda.Event(enable_timing=True, **ext) for _ in range(2)] for _ in range(steps)]
+        evp = [[torch.cuda.Event(enable_timing=True, **ext) for _ in range(4)] for _ in range(steps)]
+
+        def timed_events(i):
+            # the events step i of the timed run records: its own pair with the flush, else only
+            # the first step's start and the last step's end
+            if flushed:
+                return evs[i]
+            return [evs[0][0] if i == 0 else None, evs[-1][1] if i == steps - 1 else None]
+
+        if self.graphs:
+            g_warm, g_timed, g_parts = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+            with torch.cuda.stream(self.stream):
+                with torch.cuda.graph(g_warm, stream=self.stream):
+                    for _ in range(max(3, warmup)):
+                        self.step()
+                with torch.cuda.graph(g_timed, stream=self.stream):
+                    for i in range(steps):
+                        self.step(timed_events(i))
+                with torch.cuda.graph(g_parts, stream=self.stream):
+                    for i in range(steps):
+                        self.step(evp[i])
+            g_warm.replay()
+        else:
+            for _ in range(max(3, warmup)):
+                self.step()
+        torch.cuda.synchronize()
+        status = self.sk.sk_get_device_status(clear=True)
+        if status:
+            raise RuntimeError(f"device status {status:#x} after warm-up ({self.w.name})")
+        if ws > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        if self.graphs:
+            g_timed.replay()
+        else:
+            for i in range(steps):
+                self.step(timed_events(i))
+        torch.cuda.synchronize()
+        if ws > 1:
+            torch.distributed.barrier()
+        # the per-kernel split: the same steps again, with an event pair around each kernel
+        if self.graphs:
+            g_parts.replay()
+        else:
+            for i in range(steps):
+                self.step(evp[i])
+        torch.cuda.synchronize()
+        clocks = sampler.stop() if sampler else None
+        if self.sk.sk_get_device_status(clear=True):
+            raise RuntimeError(f"device status set during the timed steps ({self.w.name})")
+        local_ms = (sum(e[0].elapsed_time(e[1]) for e in evs) if flushed
+                    else evs[0][0].elapsed_time(evs[-1][1]))
+        return {"local_ms": local_ms, "plan_ms": [e[0].elapsed_time(e[1]) for e in evp],
+                "attn_ms": [e[1].elapsed_time(e[2]) for e in evp],
+                "merge_ms": [e[2].elapsed_time(e[3]) for e in evp], "clocks": clocks}
+
+    def attention_bytes(self):
+        """Algorithmic bytes of one attention launch: K/V once, Q once, partials written;
+        and the number of work items (planned split)."""
+        w = self.w
+        q_bytes = w.num_tokens * w.num_q_heads * w.head_dim * 2
+        items = None
+        if self.use_plan:
+            p_np = self.plan.cpu().numpy()
+            items = int((p_np[1:] >= 0).sum())
+            seg_rows = int(self.tok.cpu().numpy().astype(np.int64).sum())
+        else:
+            seg_rows = w.num_tokens * self.fixed
+        part_bytes = seg_rows * w.num_q_heads * (w.head_dim + 2) * 4
+        return w.kv_bytes + q_bytes + part_bytes, items
+
+    def launch_mode(self):
+        if self.graphs:
+            return ("timed steps replayed as one CUDA graph (one event pair around the back-to-back steps, "
+                    "or around each step when L2 is flushed between steps; the per-kernel split comes from a "
+                    "second replay with events around each kernel)")
+        return "eager, one Python call per kernel"
+
+
+def _kernel_summary(t, steps, kv_bytes):
+    """Per-kernel means (us) and KV TB/s of a PathBench.run result."""
+    am = [x + y for x, y in zip(t["attn_ms"], t["merge_ms"])]
+    ms = t["local_ms"] / steps
+    return {"ms_per_step": round(ms, 5), "us_attention": round(1e3 * statistics.mean(t["attn_ms"]), 2),
+            "us_merge": round(1e3 * statistics.mean(t["merge_ms"]), 2),
+            "us_plan": round(1e3 * statistics.mean(t["plan_ms"]), 2),
+            "us_per_call": round(1e3 * statistics.mean(am), 2),
+            "kv_tbps_step": round(kv_bytes / (ms * 1e-3) / 1e12, 4),
+            "kv_tbps_attention_plus_merge": round(kv_bytes / (1e-3 * statistics.mean(am)) / 1e12, 4)}
+
+
+PER_CONFIG = (1, 3, 4, 5, 6, 7, 8)
+
+
+def run_per_config(a, sk, torch, dev, local, main=None):
+    """Every other workload on the same box, timed as the headline one (same graph
+    replay, steps and warm-up; no CPU or e2e legs), one workload in memory at a
+    time.  Returns {config index: summary}; ``main`` is the headline's own summary,
+    used for the skew-vs-uniform ratios."""
+    peak, peak_kind = _peaks()
+    res = {}
+    for idx in PER_CONFIG:
+        if idx == a.config:
+            continue
+        w = si.config(idx)
+        pb = PathBench(sk, torch, w, dev, eager=a.eager)
+        t = pb.run(a.steps, a.warmup, 1, ClockSampler(local))
+        attn_bytes, items = pb.attention_bytes()
+        summ = _kernel_summary(t, a.steps, w.kv_bytes)
+        achieved = attn_bytes / (statistics.mean(t["attn_ms"]) * 1e-3) / 1e9
+        summ.update({"workload": w.name, "split": "plan" if pb.use_plan else "fixed", "work_items": items,
+                     "kv_dtype": "fp8_e4m3" if w.kv_dtype else "bf16", "kv_bytes_per_call": w.kv_bytes,
+                     "l2": "flushed before every step" if pb.flush is not None else "inputs larger than L2",
+                     "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                                  "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                                  "frac_of_8tbps_nominal": round(achieved / 8000.0, 4),
+                                  "algorithmic_bytes_per_launch": int(attn_bytes)},
+                     "clocks": t["clocks"], "gpu_launches": a.steps * (3 if pb.use_plan else 2)})
+        res[str(idx)] = summ
+        del pb
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return res
+
+
 def run_sk(a, w, ws, rank, local):
     import torch
     import paged_split_kv_gb300 as sk
@@ -357,134 +576,13 @@ def run_sk(a, w, ws, rank, local):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
-    q = si.make_q(w, dev)
-    kv = si.make_kv(w, dev)
-    bt = torch.as_tensor(w.block_table, device=dev)
-    lens = torch.as_tensor(w.seq_lens, device=dev)
-    cu = torch.as_tensor(w.cu_q, device=dev)
-    use_plan = w.bs > 1 and not a.fixed_split
-    nsm = w.num_sms
-    hkv = w.num_kv_heads
-    nt = w.num_tokens
-    plan = torch.empty(sk.plan_capacity(w.bs, hkv, nsm), dtype=torch.int32, device=dev) if use_plan else None
-    tok = torch.empty(nt, dtype=torch.int32, device=dev) if use_plan else None
-    part_o = torch.empty((nt, w.seg_max, w.num_q_heads, w.head_dim), dtype=torch.float32, device=dev)
-    part_m = torch.empty((nt, w.seg_max, w.num_q_heads), dtype=torch.float32, device=dev)
-    part_l = torch.empty((nt, w.seg_max, w.num_q_heads), dtype=torch.float32, device=dev)
-    out = torch.empty((nt, w.num_q_heads, w.head_dim), dtype=torch.bfloat16, device=dev)
-    lse = torch.empty((nt, w.num_q_heads), dtype=torch.float32, device=dev)
-    fixed = 0 if use_plan else sk.sk_fixed_nseg(w.bs, hkv, nsm, w.seg_max)
-    # L2 flush for inputs that fit in L2: a write larger than L2, then a read of another buffer larger
-    # than L2, which evicts the written (dirty) lines, so that their write-backs to HBM happen in the
-    # flush and not inside the timed step
-    flush = None if w.kv_bytes > 129e6 else torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    flush_rd = None if flush is None else torch.ones(256 << 20, dtype=torch.uint8, device=dev)
-    flush_sink = None if flush is None else torch.zeros(1, dtype=torch.int64, device=dev)
-    # The timed steps are captured once as a CUDA graph (every call is capture safe) and replayed
-    # once: the device runs exactly the kernels of K eager steps, but the timing does not depend
-    # on how fast the host can issue the calls.  Inputs larger than L2 run the K steps back to
-    # back between one event pair (an event between two steps would cut the overlap of one
-    # step's last kernel with the next step's first launch, ~5 us per step); with the L2 flush,
-    # each step has its own pair, so the flushes stay out of the sum.  A second graph of the same
-    # steps, with events around each kernel, gives the per-kernel split.  --eager keeps the
-    # Python-launched loops.
-    try:
-        graph_events = not a.eager and torch.cuda.Event(enable_timing=True, external=True) is not None
-    except TypeError:                      # a PyTorch without graph-recorded events
-        graph_events = False
-    stream = torch.cuda.Stream(device=dev) if graph_events else torch.cuda.current_stream()
-
-    def step(ev=None):
-        # ev: None, [start, end] of the step, or [start, after plan, after attention, end].  Events
-        # between kernels cut the launch overlap of dependent kernels, so the timed steps carry the
-        # pair only and a second replay of the same steps gives the per-kernel split.
-        parts = ev is not None and len(ev) == 4
-        if flush is not None:
-            flush.fill_(1)
-            torch.sum(flush_rd.view(torch.int64), dim=0, keepdim=True, out=flush_sink)
-        if ev is not None and ev[0] is not None:
-            ev[0].record(stream)
-        if use_plan:
-            sk.sk_plan_cache_reset()
-            sk.sk_build_plan(lens, cu, hkv, plan, tok, nsm, w.seg_max, stream)
-        if parts:
-            ev[1].record(stream)
-        sk.sk_paged_decode_attn(q, kv, bt, lens, cu, plan, part_o, part_m, part_l,
-                                max_q_len=w.max_q_len, sm_scale=w.sm_scale, num_sms=nsm,
-                                k_scale=w.k_scale, v_scale=w.v_scale, causal=bool(w.causal),
-                                stream=stream)
-        if parts:
-            ev[2].record(stream)
-        sk.sk_merge_segments(part_o, part_m, part_l, tok, out, lse, fixed_nseg=fixed, stream=stream)
-        if ev is not None and ev[-1] is not None:
-            ev[-1].record(stream)
-
-    def timed_events(i):
-        # the events step i of the timed run records: its own pair with the flush, else only
-        # the first step's start and the last step's end
-        if flush is not None:
-            return evs[i]
-        return [evs[0][0] if i == 0 else None, evs[-1][1] if i == a.steps - 1 else None]
-
-    sampler = ClockSampler(local) if rank == 0 else None
-    if sampler:
-        sampler.start()
-    stream.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            step()
-    torch.cuda.synchronize()
-    if graph_events:
-        evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)] for _ in range(a.steps)]
-        evp = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)] for _ in range(a.steps)]
-        g_warm, g_timed, g_parts = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-        with torch.cuda.stream(stream):
-            with torch.cuda.graph(g_warm, stream=stream):
-                for _ in range(max(3, a.warmup)):
-                    step()
-            with torch.cuda.graph(g_timed, stream=stream):
-                for i in range(a.steps):
-                    step(timed_events(i))
-            with torch.cuda.graph(g_parts, stream=stream):
-                for i in range(a.steps):
-                    step(evp[i])
-        g_warm.replay()
-    else:
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(a.steps)]
-        evp = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(a.steps)]
-        for _ in range(max(3, a.warmup)):
-            step()
-    torch.cuda.synchronize()
-    status = sk.sk_get_device_status(clear=True)
-    if status:
-        raise RuntimeError(f"device status {status:#x} after warm-up")
-
-    if ws > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    if graph_events:
-        g_timed.replay()
-    else:
-        for i in range(a.steps):
-            step(timed_events(i))
-    torch.cuda.synchronize()
-    if ws > 1:
-        torch.distributed.barrier()
-    # the per-kernel split: the same steps again, with an event pair around each kernel
-    if graph_events:
-        g_parts.replay()
-    else:
-        for i in range(a.steps):
-            step(evp[i])
-    torch.cuda.synchronize()
-    clocks = sampler.stop() if sampler else None
-    plan_ms = [e[0].elapsed_time(e[1]) for e in evp]
-    attn_ms = [e[1].elapsed_time(e[2]) for e in evp]
-    merge_ms = [e[2].elapsed_time(e[3]) for e in evp]
-    # with a flush, the timed region is the steps themselves (each ev[0] -> ev[1]), flushes excluded
-    local_ms = (sum(e[0].elapsed_time(e[1]) for e in evs) if flush is not None
-                else evs[0][0].elapsed_time(evs[-1][1]))
-    total_ms = max_over_ranks(local_ms, ws, dev)
+    pb = PathBench(sk, torch, w, dev, fixed_split=a.fixed_split, eager=a.eager)
+    use_plan, nsm = pb.use_plan, w.num_sms
+    q, kv, bt, lens, cu, out, lse = pb.q, pb.kv, pb.bt, pb.lens, pb.cu, pb.out, pb.lse
+    t = pb.run(a.steps, a.warmup, ws, ClockSampler(local) if rank == 0 else None)
+    clocks = t["clocks"]
+    plan_ms, attn_ms, merge_ms = t["plan_ms"], t["attn_ms"], t["merge_ms"]
+    total_ms = max_over_ranks(t["local_ms"], ws, dev)
     ms_per_step = total_ms / a.steps
     value = weak_scaling_tbps(w.kv_bytes, a.steps, ws, total_ms)
 
@@ -542,26 +640,17 @@ def run_sk(a, w, ws, rank, local):
 
     attn_avg = statistics.mean(attn_ms)
     peak, peak_kind = _peaks()
-    q_bytes = nt * w.num_q_heads * w.head_dim * 2
-    # algorithmic bytes of one attention launch: K/V once, Q once, partials written
-    rows_written = int(sum(int(w.q_lens[s]) * w.num_q_heads for s in range(w.bs)))
-    nseg_items = None
-    if use_plan:
-        p_np = plan.cpu().numpy()
-        tok_np = tok.cpu().numpy()
-        nseg_items = int((p_np[1:] >= 0).sum())
-        part_bytes = int(sum(int(tok_np[t]) for t in range(nt))) * w.num_q_heads * (w.head_dim + 2) * 4
-    else:
-        part_bytes = rows_written * fixed * (w.head_dim + 2) * 4
-    attn_bytes = w.kv_bytes + q_bytes + part_bytes
+    attn_bytes, nseg_items = pb.attention_bytes()
     achieved = attn_bytes / (attn_avg * 1e-3) / 1e9
     sha = _kernel_sources_sha()
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                "frac": round(achieved / peak, 4), "peak_kind": peak_kind + " (a copy: every byte read and written)",
+                "frac_of_8tbps_nominal": round(achieved / 8000.0, 4),
                 "traffic": _ncu_traffic(w.name, sha), "kernel": "sk attention (split-KV, paged)",
                 "algorithmic_bytes_per_launch": int(attn_bytes), "source_sha": sha}
 
     cpu = None
+    gather = None
     if not a.no_cpu_baseline and ws == 1:
         q_bits = q.view(torch.int16).cpu().numpy().view(np.uint16)
 
@@ -573,6 +662,23 @@ def run_sk(a, w, ws, rank, local):
             return sub.numpy() if w.kv_dtype == si.KV_FP8 else sub.view(torch.int16).numpy().view(np.uint16)
         cpu = _cpu_baseline(w, a.cpu_seconds, from_device=(q_bits, gather))
 
+    launch = pb.launch_mode()
+    per_config, skew = None, None
+    if ws == 1 and not a.no_per_config:
+        main = _kernel_summary(t, a.steps, w.kv_bytes)
+        # free this workload's device memory before the next one is generated
+        pb = q = kv = bt = lens = cu = out = lse = gather = None
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        per_config = run_per_config(a, sk, torch, dev, local)
+        pair = {2: main} if a.config == 2 else ({3: main} if a.config == 3 else {})
+        uni = pair.get(2) or per_config.get("2")
+        sk3 = pair.get(3) or per_config.get("3")
+        if uni and sk3:
+            skew = {"attention_plus_merge": round(sk3["kv_tbps_attention_plus_merge"]
+                                                  / uni["kv_tbps_attention_plus_merge"], 4),
+                    "step": round(sk3["kv_tbps_step"] / uni["kv_tbps_step"], 4),
+                    "definition": "KV TB/s of the agentic skew batch / KV TB/s of the uniform batch"}
     line = {"metric": METRIC, "value": round(value, 4), "unit": "TB/s", "n_gpus": ws, "steps": a.steps,
             "warmup": a.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.kv_dtype == si.KV_BF16 else "fp8_e4m3",
@@ -585,12 +691,10 @@ def run_sk(a, w, ws, rank, local):
             "kv_tbps_attention_plus_merge": round(w.kv_bytes / (1e-3 * statistics.mean(
                 [x + y for x, y in zip(attn_ms, merge_ms)])) / 1e12, 4),
             "frac_of_8tbps_nominal": round(value / 8.0, 4),
+            "per_config": per_config, "skew_vs_uniform": skew,
             "roofline": roofline, "clocks": clocks, "e2e": e2e, "e2e_serving": e2e_serving, "cpu_baseline": cpu,
             "gpu_launches": a.steps * (3 if use_plan else 2),
-            "launch": ("timed steps replayed as one CUDA graph (one event pair around the back-to-back steps, "
-                       "or around each step when L2 is flushed between steps; the per-kernel split comes from a "
-                       "second replay with events around each kernel)") if graph_events
-                      else "eager, one Python call per kernel"}
+            "launch": launch}
     print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
@@ -706,7 +810,8 @@ def _back_to_back_ms(torch, f, steps):
 
 def run_kv_write(a, local):
     """The KV write step on a prefill-sized chunk: 65536 new tokens x 8 KV heads
-    scattered into shuffled page rows (256 MB of bf16 K/V in, larger than L2)."""
+    written into standard pages at randomly permuted slots (256 MB of bf16 K/V in,
+    larger than L2)."""
     import torch
     import paged_split_kv_gb300 as sk
     if not os.path.exists(sk.LIB_PATH):

@@ -169,7 +169,7 @@ def make_workload(name: str, seq_lens, q_lens, num_q_heads: int, num_kv_heads: i
 
 
 def config(index: int) -> Workload:
-    """The five benchmark workloads, numbered 1..5 (seed = 1000 + index).
+    """The benchmark workloads, numbered 1..8 (seed = 1000 + index).
 
     1 tiny decode      bs 2, L {5, 300}, q 1, 8/1 heads, bf16
     2 uniform verify   bs 16 x 119000, q 4, 32/2 heads, bf16
@@ -179,6 +179,9 @@ def config(index: int) -> Workload:
     5 high-batch       bs 128 x 8192, q 1, 32/8 heads, bf16
     6 bs1 long         bs 1 x 110000, q 4, 32/2 heads, bf16 (the fixed-split bypass)
     7 bs1 longest      bs 1 x 248000, q 4, 32/2 heads, bf16 (the fixed-split bypass)
+    8 uniform fp8      bs 16 x 119000, q 4, 32/2 heads, fp8 e4m3 KV (k_scale 0.5, v_scale 0.25):
+                       workload 2 on e4m3 pages, 64 query rows per work item (about 512 KV
+                       bytes per token, as in the page's benchmark rows)
     """
     seed = 1000 + index
     rng = np.random.default_rng(seed)
@@ -200,6 +203,9 @@ def config(index: int) -> Workload:
         return make_workload("bs1_long_110k_q4", [110000], 4, 32, 2, seed, rng=rng)
     if index == 7:
         return make_workload("bs1_long_248k_q4", [248000], 4, 32, 2, seed, rng=rng)
+    if index == 8:
+        return make_workload("uniform_verify_16x119k_q4_fp8", [119000] * 16, 4, 32, 2, seed,
+                             kv_dtype=KV_FP8, k_scale=0.5, v_scale=0.25, rng=rng)
     raise ValueError(f"no workload {index}")
 
 

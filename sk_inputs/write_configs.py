@@ -1,5 +1,5 @@
 """Writes sk_inputs/configs.json: the sequence lengths, query lengths and shapes of
-the seven benchmark workloads as the seeded generator produces them, so the
+the eight benchmark workloads as the seeded generator produces them, so the
 workloads can be read without running anything and a test can check that the
 generator still reproduces them.
 
@@ -26,7 +26,7 @@ def describe(index: int) -> dict:
 
 
 def main():
-    out = {"workloads": [describe(i) for i in range(1, 8)]}
+    out = {"workloads": [describe(i) for i in range(1, 9)]}
     with open(os.path.join(HERE, "configs.json"), "w") as f:
         json.dump(out, f, indent=1)
         f.write("\n")

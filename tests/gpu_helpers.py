@@ -92,35 +92,52 @@ def oracle_problem(pr):
     return out.reshape(pr.num_tokens, pr.num_q_heads, pr.head_dim), lse.reshape(pr.num_tokens, pr.num_q_heads)
 
 
-def oracle_sampled(w, q, kv, seqs, rows_per_seq, rng):
-    """Oracle output for sampled rows of full-size workload ``w``: each chosen
-    sequence is copied out alone (its pages, a fresh block table) and the oracle
-    evaluates a few (token, head) rows of it.  Returns [(t, hq, out[D], lse)]."""
-    res = []
+def oracle_rows(w, q, kv, s, picks):
+    """Oracle output for the (query token j, query head hq) rows ``picks`` of
+    sequence ``s`` of full-size workload ``w``: the sequence is copied out alone
+    (its pages, a fresh block table) and the oracle evaluates only those rows.
+    Returns [(t, hq, out[D], lse)] with t the global token index."""
+    L = int(w.seq_lens[s])
+    qs = int(w.q_lens[s])
     cu = w.cu_q
+    npg = (L + w.page - 1) // w.page
+    blocks = torch.as_tensor(w.block_table[s, :npg].astype(np.int64), device=kv.device)
+    kv_sub = kv.index_select(0, blocks) if npg else kv[:0]
+    q_sub = q[cu[s]:cu[s] + qs]
+    q_bits, kv_bits = host_bits(q_sub, kv_sub, w.kv_dtype)
+    if npg == 0:
+        kv_bits = np.zeros((1,) + tuple(kv.shape[1:]), dtype=kv_bits.dtype)
+    bt = np.arange(max(npg, 1), dtype=np.int32)[None, :]
+    picks = sorted(set(picks))
+    rows = np.array([j * w.num_q_heads + h for j, h in picks], dtype=np.int64)
+    out, lse = oracle.attention(q_bits, kv_bits, w.kv_dtype, w.k_scale, w.v_scale, bt, w.page,
+                                np.array([L], np.int32), np.array([0, qs], np.int32),
+                                w.num_q_heads, w.num_kv_heads, w.head_dim, w.sm_scale, w.causal,
+                                rows=rows)
+    return [(int(cu[s]) + j, h, o, l) for (j, h), o, l in zip(picks, out, lse)]
+
+
+def oracle_sampled(w, q, kv, seqs, rows_per_seq, rng):
+    """Oracle output for a few random (token, head) rows of each sequence in
+    ``seqs`` of full-size workload ``w``.  Returns [(t, hq, out[D], lse)]."""
+    res = []
     for s in seqs:
-        L = int(w.seq_lens[s])
         qs = int(w.q_lens[s])
         if qs == 0:
             continue
-        npg = (L + w.page - 1) // w.page
-        blocks = torch.as_tensor(w.block_table[s, :npg].astype(np.int64), device=kv.device)
-        kv_sub = kv.index_select(0, blocks) if npg else kv[:0]
-        q_sub = q[cu[s]:cu[s] + qs]
-        q_bits, kv_bits = host_bits(q_sub, kv_sub, w.kv_dtype)
-        if npg == 0:
-            kv_bits = np.zeros((1,) + tuple(kv.shape[1:]), dtype=kv_bits.dtype)
-        bt = np.arange(max(npg, 1), dtype=np.int32)[None, :]
         picks = [(int(rng.integers(0, qs)), int(rng.integers(0, w.num_q_heads))) for _ in range(rows_per_seq)]
-        picks = sorted(set(picks))
-        rows = np.array([j * w.num_q_heads + h for j, h in picks], dtype=np.int64)
-        out, lse = oracle.attention(q_bits, kv_bits, w.kv_dtype, w.k_scale, w.v_scale, bt, w.page,
-                                    np.array([L], np.int32), np.array([0, qs], np.int32),
-                                    w.num_q_heads, w.num_kv_heads, w.head_dim, w.sm_scale, w.causal,
-                                    rows=rows)
-        for (j, h), o, l in zip(picks, out, lse):
-            res.append((int(cu[s]) + j, h, o, l))
+        res += oracle_rows(w, q, kv, s, picks)
     return res
+
+
+def row_relative_error(got_row, ref_row):
+    """max |got - ref| over a row divided by max |ref| of that row (0 for an all-zero
+    reference that the kernel also returned as zeros)."""
+    scale = float(np.max(np.abs(ref_row)))
+    err = float(np.max(np.abs(np.asarray(got_row, np.float64) - ref_row)))
+    if scale == 0.0:
+        return 0.0 if err == 0.0 else float("inf")
+    return err / scale
 
 
 def oracle_all_rows(w, q, kv):

@@ -182,7 +182,7 @@ def _run_workload(w, dev, use_plan=True):
     return q, kv, run_library(w, q, kv, use_plan=use_plan)
 
 
-@pytest.mark.parametrize("idx", [1, 2, 3, 4, 5, 6, 7])
+@pytest.mark.parametrize("idx", [1, 2, 3, 4, 5, 6, 7, 8])
 def test_full_workload_sampled_rows(idx):
     w = si.config(idx)
     dev = torch.device(DEV)
