@@ -75,6 +75,10 @@ constexpr int kSoftmaxWarp0 = 2;
 constexpr long long kDrainLimit = 4000000000LL;     // cycles (~2 s): waits for work already issued
 constexpr uint32_t kFull = 0xffffffffu;
 constexpr int kMaxSmem = 232448;                    // 227 KB per CTA
+// e4m3 path: the subtrahend of a row whose running max is still -inf.  Any visible score then
+// gives d = s * c - msub far above the rescale threshold (f16 +inf), so the running max is set
+// before any P of that row is formed; a masked score gives -inf - msub = -inf, p = 0.
+constexpr float kMsubNone = -0x1p100f;
 
 // Stage layout.  One TMA copy per page brings its 16 token rows as two 8-token
 // groups, each group as its 128-byte chunks of the row, each chunk an 8 x 128 B
@@ -241,6 +245,68 @@ __device__ __forceinline__ float f16lo_to_float(uint32_t v)
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
 {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// Two floats to a packed f16 pair (lo in the low half), round to nearest even.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t hmax2(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("max.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// lo += low half of v, hi += high half of v (f16 added into fp32, one rounding each).
+__device__ __forceinline__ void add_f16x2_to_f32(uint32_t v, float &lo, float &hi)
+{
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\tadd.rn.f32.f16 %0, a, %0;\n\tadd.rn.f32.f16 %1, b, %1;\n\t}"
+        : "+f"(lo), "+f"(hi)
+        : "r"(v));
+}
+
+// 2^x of both halves on the special-function unit (half precision).
+__device__ __forceinline__ uint32_t ex2_f16x2(uint32_t x)
+{
+    uint32_t r;
+    asm("ex2.approx.f16x2 %0, %1;" : "=r"(r) : "r"(x));
+    return r;
+}
+
+// Whether either half of a packed f16 pair exceeds `thr`.
+__device__ __forceinline__ bool f16x2_any_gt(uint32_t v, float thr)
+{
+    float lo, hi;
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(v));
+    return fmaxf(lo, hi) > thr;
+}
+
+// Two packed f16 pairs to four e4m3 codes (a's low half in the low byte, then a's high
+// half, b's low, b's high), nearest even, saturated to +-448.
+__device__ __forceinline__ uint32_t e4m3x4_from_f16x2(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f16x2 lo, %1;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f16x2 hi, %2;\n\t"
+        "mov.b32 %0, {lo, hi};\n\t}"
+        : "=r"(r)
+        : "r"(a), "r"(b));
+    return r;
 }
 
 template <int RP, bool FP8>
@@ -433,7 +499,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             reinterpret_cast<long long *>(misc + C::kSlot)[r] = slot;
             m_run[r] = -CUDART_INF_F;
             m_thr[r] = -CUDART_INF_F;
-            m_sub[r] = 0.f;
+            m_sub[r] = FP8 ? kMsubNone : 0.f;
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -618,6 +684,349 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                 mbar_wait_bounded(bar_odone, 0, nullptr, kDrainLimit);
         }
         __syncwarp();
+    } else if constexpr (FP8) {
+        // ================================================================ softmax warpgroups, e4m3 pages
+        // Group g owns query rows [g*RH, (g+1)*RH) and each thread the two tokens tau and 128 + tau
+        // of the tile (its TMEM lane in each half).  Per score the work is kept to a few
+        // instructions, since with 64 rows this path is bound by instruction issue:
+        //   d = s * c_r - msub_r      one FFMA (c_r: the row's score scale in log2 units, Q's
+        //                             power-of-two row scale included; msub_r: its running max
+        //                             less kPShift), packed in pairs to f16;
+        //   rescale vote              one packed max per pair: the running max moves only when
+        //                             some d exceeds kThrLog2 + kPShift (p would pass 2^8);
+        //   p * 2^kPShift = 2^d       one ex2.approx.f16x2 per pair;
+        //   hi, lo                    hi = p with 3 fraction bits (a mask), lo = p - hi (exact
+        //                             in f16), each then one e4m3 code: p = hi + lo within 2^-8;
+        //   row sums                  the two tokens' p of a row pair added in f16 (one packed
+        //                             add per two pairs), then added into the fp32 sums by two
+        //                             mixed-precision adds.
+        // The f16 exponential's own error (about 2^-10) is below the split's.  (Row sums taken on
+        // the tensor cores instead, as ones . P^T beside O, cost more than they saved: the
+        // extra products lengthened every stage's life.)
+        constexpr int RH = C::kRH;
+        constexpr int NH = C::kHalves;
+        constexpr int NP = RH / 2;                             // f16 pairs of rows per half
+        constexpr int kLd = RH >= 32 ? 32 : RH;                // TMEM columns per load
+        static_assert(kLd % 4 == 0 && RH % 8 == 0, "the epilogue transposes blocks of four rows");
+        const int wg = (warp - kSoftmaxWarp0) >> 2;            // softmax group
+        const int tw = (warp - kSoftmaxWarp0) & 3;             // warp within the group
+        const int r0 = wg * RH;                                // first row of the group
+        const uint32_t bar_id = 1 + wg;                        // named barrier of the group
+        const int quarter = warp & 3;                          // TMEM lane quarter this warp may access
+        const int tau = quarter * 32 + lane;                   // token row (S) / dimension (O) of this thread
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const int tid = tw * 32 + lane;
+        const int causal_base = w.L - w.q_len;
+        const int last_page_end = (w.L + kPage - 1) / kPage * kPage;
+        bool failed = false;
+        float *gred = red + wg * (4 * 32);
+        float lsum[RH];
+#pragma unroll
+        for (int r = 0; r < RH; ++r)
+            lsum[r] = 0.f;
+
+        // S of this thread's tokens (the stacked hi | lo Q terms summed)
+        auto load_scores = [&](int sb, float (&x)[NH][RH]) {
+#pragma unroll
+            for (int hf = 0; hf < NH; ++hf) {
+                const uint32_t s_col = tmem_s0 + sb * C::kSBufCols + hf * C::kSCols + r0 + lane_off;
+#pragma unroll
+                for (int c = 0; c < RH; c += kLd)
+                    tmem_ld32<kLd>(s_col + c, x[hf] + c);
+            }
+            if constexpr (C::kStackQ) {
+                float y[NH][RH];
+#pragma unroll
+                for (int hf = 0; hf < NH; ++hf) {
+                    const uint32_t s_col = tmem_s0 + sb * C::kSBufCols + hf * C::kSCols + RP + r0 + lane_off;
+#pragma unroll
+                    for (int c = 0; c < RH; c += kLd)
+                        tmem_ld32<kLd>(s_col + c, y[hf] + c);
+                }
+                tmem_wait_ld();
+#pragma unroll
+                for (int hf = 0; hf < NH; ++hf)
+#pragma unroll
+                    for (int r = 0; r < RH; ++r)
+                        x[hf][r] += y[hf][r];
+            } else {
+                tmem_wait_ld();
+            }
+        };
+        // -inf where row r = j' * G + i does not see this thread's key of half hf (past the
+        // segment end, or causally ahead of query token j'); whole tiles inside both limits
+        // keep their scores (padding rows r >= R have zero Q: scores 0, never written out)
+        auto mask_scores = [&](int j, bool ok, float (&x)[NH][RH]) {
+#pragma unroll
+            for (int hf = 0; hf < NH; ++hf) {
+                const int tok = k0 + j * C::kTile + hf * kTokTile + tau;
+                const int ahead = tok - causal_base;
+                const int rmin = ((p.causal && ahead > 0) ? ahead * p.G : 0) - row0;
+                if (!(ok && tok < k1 && rmin <= 0)) {
+                    const bool tok_vis = ok && tok < k1;
+#pragma unroll
+                    for (int r = 0; r < RH; ++r) {
+                        const int rg = r0 + r;
+                        x[hf][r] = (tok_vis && rg >= rmin && rg < R) ? x[hf][r] : -CUDART_INF_F;
+                    }
+                }
+            }
+        };
+        // d = s * c - msub in f16 pairs; returns whether some d passes the rescale threshold
+        auto make_d = [&](const float (&x)[NH][RH], uint32_t (&dh)[NH][NP]) {
+            uint32_t dmax = 0xFC00FC00u;                       // (-inf, -inf)
+#pragma unroll
+            for (int r = 0; r < RH; r += 4) {
+                const float4 c = *reinterpret_cast<const float4 *>(crow + r0 + r);
+                const float4 m = *reinterpret_cast<const float4 *>(m_sub + r0 + r);
+#pragma unroll
+                for (int hf = 0; hf < NH; ++hf) {
+                    const uint32_t a = pack_f16x2(fmaf(x[hf][r], c.x, -m.x), fmaf(x[hf][r + 1], c.y, -m.y));
+                    const uint32_t b = pack_f16x2(fmaf(x[hf][r + 2], c.z, -m.z), fmaf(x[hf][r + 3], c.w, -m.w));
+                    dh[hf][r / 2] = a;
+                    dh[hf][r / 2 + 1] = b;
+                    dmax = hmax2(dmax, hmax2(a, b));
+                }
+            }
+            return f16x2_any_gt(dmax, C::kThrLog2 + (float)C::kPShift);
+        };
+
+        for (int j = 0; j < ntiles; ++j) {
+            const int sb = j % C::kSBufs;          // S buffer and its barriers
+            const int st = j % C::kStages;
+            float x[NH][RH];
+            uint32_t dh[NH][NP];
+            bool ok = !failed && mbar_wait_bounded(bar_sfull(sb), (j / C::kSBufs) & 1, abort_flag, p.wait_limit);
+            ok = __all_sync(kFull, ok);          // tcgen05.ld is warp-collective
+            if (ok) {
+                tc_fence_after();
+                load_scores(sb, x);
+            }
+            mask_scores(j, ok, x);
+            const bool big = make_d(x, dh);
+            // group decision, one reduction over the group's 128 threads: rescale needed or a wait
+            // failed?  Only then a second one tells which (every thread gets the same answers).
+            // The S buffer is released after it, so that the rare rescale can read S again.
+            if (named_bar_or(bar_id, 128, big || !ok)) {
+                if (named_bar_or(bar_id, 128, !ok)) {
+                    if (tid == 0) {
+                        *abort_flag = 1;
+                        atomicOr(p.status, SK_DEV_TIMEOUT);
+                    }
+                    failed = true;
+                    break;
+                }
+                tc_fence_after();
+                load_scores(sb, x);                // S again: no score stayed live through make_d
+                mask_scores(j, true, x);
+                // exact tile max of s * c over the group's rows across its 128 threads (c > 0)
+                constexpr int kRc = RH >= 32 ? 32 : RH;
+#pragma unroll
+                for (int c0 = 0; c0 < RH; c0 += kRc) {
+                    float v[kRc];
+#pragma unroll
+                    for (int r = 0; r < kRc; ++r) {
+                        float mx = x[0][c0 + r];
+#pragma unroll
+                        for (int hf = 1; hf < NH; ++hf)
+                            mx = fmaxf(mx, x[hf][c0 + r]);
+                        v[r] = mx * crow[r0 + c0 + r];
+                    }
+                    warp_transpose_reduce<kRc, true>(v, lane);
+                    gred[tw * 32 + c0 + reduce_row0<kRc>(lane)] = v[0];
+                }
+                named_bar_sync(bar_id, 128);
+                if (tid < RH) {
+                    const int rg = r0 + tid;
+                    const float mt = fmaxf(fmaxf(gred[tid], gred[32 + tid]), fmaxf(gred[64 + tid], gred[96 + tid]));
+                    const float mo = m_run[rg];
+                    const float mn = fmaxf(mo, mt);
+                    alpha_s[rg] = (mo == -CUDART_INF_F) ? 0.f : exp2f(mo - mn);
+                    m_run[rg] = mn;
+                    m_sub[rg] = mn == -CUDART_INF_F ? kMsubNone : mn - (float)C::kPShift;
+                }
+                named_bar_sync(bar_id, 128);
+#pragma unroll
+                for (int r = 0; r < RH; ++r)
+                    lsum[r] *= alpha_s[r0 + r];
+                if (j > 0) {
+                    // O holds tiles < j: wait for PV(j-1) (the same argument as for bf16 makes its
+                    // phase of empty[(j-1) % kStages] unambiguous), then rescale this thread's
+                    // dimension of O_hi and O_lo
+                    const int jp = j - 1;
+                    bool okp = mbar_wait_bounded(bar_empty(jp % C::kStages), (jp / C::kStages) & 1, abort_flag, p.wait_limit);
+                    okp = __all_sync(kFull, okp);    // tcgen05.ld/st are warp-collective
+                    if (okp) {
+                        tc_fence_after();
+#pragma unroll
+                        for (int blk = 0; blk < 2; ++blk) {
+#pragma unroll
+                            for (int c = 0; c < RH; c += kLd) {
+                                float o[kLd];
+                                const uint32_t col = tmem_o + blk * RP + r0 + c + lane_off;
+                                tmem_ld32<kLd>(col, o);
+                                tmem_wait_ld();
+#pragma unroll
+                                for (int r = 0; r < kLd; ++r)
+                                    o[r] *= alpha_s[r0 + c + r];
+                                tmem_st32<kLd>(col, o);
+                            }
+                        }
+                        tmem_wait_st();
+                    } else {
+                        failed = true;             // the next tile's vote takes the group out together
+                    }
+                }
+                // against the new running max (every d <= kPShift); S is read once more, so that
+                // no score stays live through the reductions and the O rescale above
+                tc_fence_after();
+                load_scores(sb, x);
+                mask_scores(j, true, x);
+                make_d(x, dh);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(bar_sfree(sb));
+            if (!failed) {
+                // P^T over the tile's K codes, which QK(j) no longer needs: MN-major, 128-byte
+                // swizzle, 16-byte unit u of token row t stored at u ^ (t % 8); row r's hi code at
+                // byte r, its lo code at byte RP + r
+#pragma unroll
+                for (int hf = 0; hf < NH; ++hf) {
+                    const int t = hf * kTokTile + tau;          // token of the tile
+                    const uint32_t prow = stage(st) + (uint32_t)((t >> 3) * C::kGroupBytes + (t & 7) * 128);
+#pragma unroll
+                    for (int u0 = 0; u0 < RH / 8; u0 += 2) {
+                        // 16 rows (8 when RH is 8): p, the row sums, the two terms' codes
+                        constexpr int kU = RH >= 16 ? 2 : 1;
+                        uint32_t hw[2 * kU], lw[2 * kU];
+#pragma unroll
+                        for (int v = 0; v < 2 * kU; ++v) {
+                            const int k = 4 * u0 + 2 * v;              // first pair: rows 2k, 2k + 1
+                            const uint32_t p0 = ex2_f16x2(dh[hf][k]), p1 = ex2_f16x2(dh[hf][k + 1]);
+                            add_f16x2_to_f32(p0, lsum[2 * k], lsum[2 * k + 1]);
+                            add_f16x2_to_f32(p1, lsum[2 * k + 2], lsum[2 * k + 3]);
+                            const uint32_t h0 = p0 & 0xFF80FF80u, h1 = p1 & 0xFF80FF80u;
+                            hw[v] = e4m3x4_from_f16x2(h0, h1);
+                            lw[v] = e4m3x4_from_f16x2(hsub2(p0, h0), hsub2(p1, h1));
+                        }
+                        if constexpr (kU == 2) {
+                            // 16 rows' codes leave as one 16-byte store per term
+                            const int bh = r0 + 8 * u0, bl = RP + bh;      // multiples of 16
+                            st_shared_v4(prow + (uint32_t)(((bh >> 4) ^ (t & 7)) << 4), hw[0], hw[1], hw[2], hw[3]);
+                            st_shared_v4(prow + (uint32_t)(((bl >> 4) ^ (t & 7)) << 4), lw[0], lw[1], lw[2], lw[3]);
+                        } else {
+                            const int bh = r0 + 8 * u0, bl = RP + r0 + 8 * u0;   // byte of the first row
+                            *reinterpret_cast<uint2 *>(smem + (prow - sbase) + (((bh >> 4) ^ (t & 7)) << 4) + (bh & 15)) =
+                                make_uint2(hw[0], hw[1]);
+                            *reinterpret_cast<uint2 *>(smem + (prow - sbase) + (((bl >> 4) ^ (t & 7)) << 4) + (bl & 15)) =
+                                make_uint2(lw[0], lw[1]);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int hf = 0; hf < NH; ++hf) {
+                    const int t = hf * kTokTile + tau;
+                    const int tok = k0 + j * C::kTile + t;
+                    if (tok >= w.L && tok < last_page_end) {
+                        // past L in the last page the row holds anything (0 * NaN would reach O): this
+                        // group's share of the token's 128 V code bytes becomes zeros
+                        constexpr int kZeroBytes = 128 / C::kGroups;
+                        uint8_t *vrow = smem + st * C::kStageBytes + C::kOffV + (t >> 3) * C::kGroupBytes + (t & 7) * 128 +
+                                        wg * kZeroBytes;
+#pragma unroll
+                        for (int u = 0; u < kZeroBytes / 16; ++u)
+                            *reinterpret_cast<uint4 *>(vrow + u * 16) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+                fence_proxy_async_smem();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(bar_pfull(sb));
+            if (failed && lane == 0)
+                *abort_flag = 1;                   // the next tile's vote propagates the failure
+        }
+
+        // ---- epilogue: row sums across the group's threads (they do not need the last PV, which
+        // completes meanwhile), then O complete? and the partials
+        {
+            constexpr int kRc = RH >= 32 ? 32 : RH;
+#pragma unroll
+            for (int c0 = 0; c0 < RH; c0 += kRc) {
+                float v[kRc];
+#pragma unroll
+                for (int r = 0; r < kRc; ++r)
+                    v[r] = lsum[c0 + r];
+                warp_transpose_reduce<kRc, false>(v, lane);
+                gred[tw * 32 + c0 + reduce_row0<kRc>(lane)] = v[0];
+            }
+        }
+        named_bar_sync(bar_id, 128);
+        if (tid < RH)
+            alpha_s[r0 + tid] = (gred[tid] + gred[32 + tid]) + (gred[64 + tid] + gred[96 + tid]);
+        bool okf = !failed;
+        if (okf && ntiles > 0)
+            okf = mbar_wait_bounded(bar_odone, 0, abort_flag, p.wait_limit);
+        // the group's verdict; the barrier also publishes the row sums written above
+        const bool write = !named_bar_or(bar_id, 128, !okf);
+        if (write) {
+            if (ntiles > 0)
+                tc_fence_after();
+            const float o_scale = p.v_scale * (1.0f / (float)(1 << C::kPShift));
+            const long long *slots = reinterpret_cast<const long long *>(misc + C::kSlot);
+#pragma unroll
+            for (int c = 0; c < RH; c += kLd) {
+                float o[kLd];
+                if (ntiles > 0) {
+                    float o2[kLd];
+                    tmem_ld32<kLd>(tmem_o + r0 + c + lane_off, o);
+                    tmem_ld32<kLd>(tmem_o + RP + r0 + c + lane_off, o2);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int r = 0; r < kLd; ++r)
+                        o[r] += o2[r];
+                } else {
+#pragma unroll
+                    for (int r = 0; r < kLd; ++r)
+                        o[r] = 0.f;
+                }
+#pragma unroll
+                for (int rr = 0; rr < kLd; ++rr)
+                    o[rr] = alpha_s[r0 + c + rr] > 0.f ? o[rr] * o_scale : 0.f;
+                // 4 x 4 transposes within lane quads: lane 4a + b ends with row 4k + b of each block of
+                // four rows and dimensions 4a .. 4a + 3 of the warp's quarter, so a warp store writes
+                // four rows of 128 contiguous bytes, 16 bytes a lane (part_o is 16-byte aligned)
+                const int qb = lane & 3;
+                const bool qb0 = (qb & 1) != 0, qb1 = (qb & 2) != 0;
+                const int dim4 = quarter * 32 + (lane & ~3);
+#pragma unroll
+                for (int k = 0; k < kLd / 4; ++k) {
+                    const float x0 = o[4 * k], x1 = o[4 * k + 1], x2 = o[4 * k + 2], x3 = o[4 * k + 3];
+                    const float own0 = qb1 ? x2 : x0, own1 = qb1 ? x3 : x1;
+                    const float rc0 = __shfl_xor_sync(kFull, qb1 ? x0 : x2, 2);
+                    const float rc1 = __shfl_xor_sync(kFull, qb1 ? x1 : x3, 2);
+                    const float zl0 = qb1 ? rc0 : own0, zl1 = qb1 ? rc1 : own1;
+                    const float zh0 = qb1 ? own0 : rc0, zh1 = qb1 ? own1 : rc1;
+                    const float rl = __shfl_xor_sync(kFull, qb0 ? zl0 : zl1, 1);
+                    const float rh = __shfl_xor_sync(kFull, qb0 ? zh0 : zh1, 1);
+                    const float kl = qb0 ? zl1 : zl0, kh = qb0 ? zh1 : zh0;
+                    const float4 y = make_float4(qb0 ? rl : kl, qb0 ? kl : rl, qb0 ? rh : kh, qb0 ? kh : rh);
+                    const int r = r0 + c + 4 * k + qb;
+                    if (r < R)
+                        *reinterpret_cast<float4 *>(p.part_o + slots[r] * kHeadDim + dim4) = y;
+                }
+            }
+            const int r = r0 + tid;
+            if (tid < RH && r < R) {
+                const long long slot = slots[r];
+                const float l = alpha_s[r] * (1.0f / (float)(1 << C::kPShift));
+                p.part_m[slot] = l > 0.f ? m_run[r] * 0.69314718055994531f : -CUDART_INF_F;
+                p.part_l[slot] = l;
+            }
+        }
     } else {
         // ================================================================ softmax warpgroups
         // Group g owns query rows [g*RH, (g+1)*RH): their S and O columns, running max, row
