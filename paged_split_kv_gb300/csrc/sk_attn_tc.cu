@@ -43,8 +43,10 @@
 // the rows are split over four softmax warpgroups (608 threads) instead of two,
 // so that a thread holds 16 rows of its two tokens.
 // QK splits Q into two e4m3 terms (q * 2^e_r = hi + lo, a power-of-two scale
-// per row): for up to 32 rows the two terms are one stacked operand (S_hi |
-// S_lo, added by the softmax), else two products into the same S.  PV splits
+// per row), stacked as one operand of 2R rows, so one product per 32
+// dimensions gives S_hi | S_lo (K read once), added by the softmax.  With 64
+// rows one S buffer of a tile is 256 TMEM columns, so there is a single one
+// (with O that is 384 of the 512 columns).  PV splits
 // P the same way (p * 2^4 = hi + lo, about 8 significant bits), stacked as
 // 2R columns of P^T, so O^T holds O_hi | O_lo, added at the end.  The scales
 // k_scale and v_scale are folded into the score scale and the output.
@@ -106,16 +108,19 @@ struct Cfg {
     static constexpr int kHalves = kTile / kTokTile;          // 128-token MMAs per tile
     static constexpr int kPagesPerTile = kTile / kPage;       // TMA copies per tile (<= 32 lanes)
     static constexpr int kStageBytes = kTile * (FP8 ? 256 : 512);
-    // S^T buffers in TMEM: QK may run this many tiles ahead of PV
-    static constexpr int kSBufs = kHalves == 2 ? 2 : 4;
+    // S^T buffers in TMEM: QK may run this many tiles ahead of the softmax (fp8 with 64 rows:
+    // one, since a stacked S buffer of a 256-token tile is 256 columns)
+    static constexpr int kSBufs = kHalves == 2 ? (RP == 64 ? 1 : 2) : 4;
     static constexpr int kStagesFit = (kMaxSmem - kQBytes - kMiscBytes) / kStageBytes;
     static constexpr int kStages = kStagesFit < 6 ? kStagesFit : 6;
     static constexpr int kOffQ = kStages * kStageBytes;
     static constexpr int kOffMisc = kOffQ + kQBytes;
     static constexpr int kSmemBytes = kOffMisc + kMiscBytes;
-    // fp8 with up to 32 rows: Q's hi and lo terms are one operand of 2*RP rows, so one product
-    // per 32 dimensions gives S_hi | S_lo side by side (K read once), summed by the softmax
-    static constexpr bool kStackQ = FP8 && RP <= 32;
+    // fp8: Q's hi and lo terms are one operand of 2*RP rows, so one product per 32 dimensions
+    // gives S_hi | S_lo side by side (K read once), summed by the softmax.  (With 64 rows as two
+    // products into one S, each tile took 16 products reading K twice: 183.6 -> 175.1 us on a
+    // 16 x 119k verify batch with the stacked operand.)
+    static constexpr bool kStackQ = FP8;
     static constexpr int kSCols = kStackQ ? 2 * RP : RP;     // TMEM columns of one S buffer
     static constexpr int kOCols = FP8 ? 2 * RP : RP;         // O^T, or O_hi^T | O_lo^T
     static constexpr int kSBufCols = kHalves * kSCols;       // one S buffer: a tile's halves side by side
@@ -138,9 +143,8 @@ struct Cfg {
     static constexpr int kBarEmpty = 8 * kStages;            // [kStages]
     static constexpr int kBarSFull = 16 * kStages;           // [kSBufs]
     static constexpr int kBarSFree = kBarSFull + 8 * kSBufs; // [kSBufs]
-    static constexpr int kBarPFull = kBarSFree + 8 * kSBufs; // [kSBufs], by S buffer
-    static constexpr int kBarPvIs = kBarPFull + 8 * kSBufs;  // [kSBufs]: the PV of a tile issued
-    static constexpr int kBarODone = kBarPvIs + 8 * kSBufs;  // committed once, after the last PV
+    static constexpr int kBarPFull = kBarSFree + 8 * kSBufs; // [kStages], by stage
+    static constexpr int kBarODone = kBarPFull + 8 * kStages; // committed once, after the last PV
     static constexpr int kTmemSlot = kBarODone + 8;
     static constexpr int kAbort = kTmemSlot + 4;
     static constexpr int kRed = 320;                         // float[group][4][32]
@@ -357,7 +361,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
     auto bar_sfull = [&](int b) { return mbase + C::kBarSFull + 8 * b; };
     auto bar_sfree = [&](int b) { return mbase + C::kBarSFree + 8 * b; };
     auto bar_pfull = [&](int b) { return mbase + C::kBarPFull + 8 * b; };
-    auto bar_pvis = [&](int b) { return mbase + C::kBarPvIs + 8 * b; };
     const uint32_t bar_odone = mbase + C::kBarODone;
     const uint32_t q_s = sbase + C::kOffQ;
     auto stage = [&](int s) { return sbase + (uint32_t)(s * C::kStageBytes); };
@@ -417,12 +420,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(bar_full(s), 1);
             mbar_init(bar_empty(s), 1);
+            mbar_init(bar_pfull(s), C::kSoftmaxWarps);
         }
         for (int b = 0; b < C::kSBufs; ++b) {
             mbar_init(bar_sfull(b), 1);
             mbar_init(bar_sfree(b), C::kSoftmaxWarps);
-            mbar_init(bar_pfull(b), C::kSoftmaxWarps);
-            mbar_init(bar_pvis(b), 1);
         }
         mbar_init(bar_odone, 1);
         *abort_flag = 0;
@@ -587,19 +589,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
         bool ok = true;
         int last = -1;
         if (warp == 1) {
-            // QK(j) once tile j has landed, its S buffer (j % kSBufs) is free, and PV(j - kSBufs)
-            // is issued.  The last condition keeps barrier phases unambiguous: P_full[b] cannot
-            // run a full round of buffers ahead of its PV.  The two conditions on tile
-            // j - kSBufs are checked first, while tile j is still in flight, so that once it
-            // lands only its own wait stands before the products (an mbarrier check can take
-            // hundreds of cycles while the softmax warps keep shared memory busy: fp8
-            // draft-extend 202.2 -> 198.5 us per step).  Neither condition depends on tile j.
+            // QK(j) once tile j has landed and its S buffer (j % kSBufs) is free.  The buffer's
+            // condition is checked first, while tile j is still in flight, so that once it lands
+            // only its own wait stands before the products (an mbarrier check can take hundreds
+            // of cycles while the softmax warps keep shared memory busy).  P_full is indexed by
+            // stage, so it cannot run ahead of its PV: tile j + kStages reuses the stage only after
+            // PV(j) has completed.
             for (int j = 0; j < ntiles && ok; ++j) {
                 const int st = j % C::kStages, b = j % C::kSBufs;
                 if (j >= C::kSBufs)
                     ok = mbar_wait_bounded(bar_sfree(b), ((j / C::kSBufs) - 1) & 1, abort_flag, p.wait_limit);
-                if (ok && j >= C::kSBufs)     // PV(j - kSBufs) issued: phase j / kSBufs - 1 of pvis[b]
-                    ok = mbar_wait_bounded(bar_pvis(b), ((j / C::kSBufs) - 1) & 1, abort_flag, p.wait_limit);
                 if (ok)
                     ok = mbar_wait_bounded(bar_full(st), (j / C::kStages) & 1, abort_flag, p.wait_limit);
                 ok = __all_sync(kFull, ok);
@@ -648,7 +647,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             // PV(i) as soon as the softmax threads have written P(i).  Its completion frees the
             // stage (empty), which is also how the softmax learns that O holds tile i.
             for (int i = 0; i < ntiles && ok; ++i) {
-                ok = mbar_wait_bounded(bar_pfull(i % C::kSBufs), (i / C::kSBufs) & 1, abort_flag, p.wait_limit);
+                ok = mbar_wait_bounded(bar_pfull(i % C::kStages), (i / C::kStages) & 1, abort_flag, p.wait_limit);
                 ok = __all_sync(kFull, ok);
                 if (!ok)
                     break;
@@ -667,9 +666,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                 }
                 mma_commit_warp(bar_empty(i % C::kStages));
                 last = i;
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(bar_pvis(i % C::kSBufs));
             }
             if (last >= 0)
                 mma_commit_warp(bar_odone);   // completes once every PV issued has completed
@@ -733,25 +729,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
 #pragma unroll
                 for (int c = 0; c < RH; c += kLd)
                     tmem_ld32<kLd>(s_col + c, x[hf] + c);
-            }
-            if constexpr (C::kStackQ) {
-                float y[NH][RH];
-#pragma unroll
-                for (int hf = 0; hf < NH; ++hf) {
-                    const uint32_t s_col = tmem_s0 + sb * C::kSBufCols + hf * C::kSCols + RP + r0 + lane_off;
+                if constexpr (C::kStackQ) {
+                    // S_hi | S_lo side by side: one half's lo columns at a time keeps registers low
+                    float y[RH];
 #pragma unroll
                     for (int c = 0; c < RH; c += kLd)
-                        tmem_ld32<kLd>(s_col + c, y[hf] + c);
-                }
-                tmem_wait_ld();
-#pragma unroll
-                for (int hf = 0; hf < NH; ++hf)
+                        tmem_ld32<kLd>(s_col + RP + c, y + c);
+                    tmem_wait_ld();
 #pragma unroll
                     for (int r = 0; r < RH; ++r)
-                        x[hf][r] += y[hf][r];
-            } else {
-                tmem_wait_ld();
+                        x[hf][r] += y[r];
+                }
             }
+            if constexpr (!C::kStackQ)
+                tmem_wait_ld();
         };
         // -inf where row r = j' * G + i does not see this thread's key of half hf (past the
         // segment end, or causally ahead of query token j'); whole tiles inside both limits
@@ -945,7 +936,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(bar_pfull(sb));
+                mbar_arrive(bar_pfull(st));
             if (failed && lane == 0)
                 *abort_flag = 1;                   // the next tile's vote propagates the failure
         }
@@ -1278,7 +1269,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(bar_pfull(sb));
+                mbar_arrive(bar_pfull(st));
             if (failed) {
                 // the next tile's group decision propagates the failure
                 *abort_flag = 1;
