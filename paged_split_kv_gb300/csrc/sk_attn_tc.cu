@@ -33,6 +33,9 @@
 //            tile; only then is the tile max reduced across the 128 threads
 //            and O rescaled (which waits for the previous PV).
 //            Row sums are kept per thread and reduced once at the end.
+//            On e4m3 pages the per-score work runs in packed f16 (d = s * c -
+//            msub by FFMA, ex2.f16x2 on pairs, the rescale vote from a packed
+//            max, the two e4m3 terms of P from a mask and a packed subtract).
 //            P^T is written over the tile's own K area, which QK no longer
 //            needs, so every stage carries its own P buffer.  At the end the
 //            same warps move O^T from TMEM into the partials, 16 bytes a lane
@@ -138,6 +141,7 @@ struct Cfg {
     // in the partials.
     static constexpr float kThrLog2 = FP8 ? 4.0f : 8.0f;
     static constexpr int kPShift = FP8 ? 4 : 0;
+    static_assert(kPShift >= 0 && kPShift < 8, "P * 2^kPShift stays inside the e4m3 range");
     // misc area
     static constexpr int kBarFull = 0;                       // [kStages]
     static constexpr int kBarEmpty = 8 * kStages;            // [kStages]
@@ -1019,7 +1023,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             }
         }
     } else {
-        // ================================================================ softmax warpgroups
+        // ================================================================ softmax warpgroups, bf16 pages
         // Group g owns query rows [g*RH, (g+1)*RH): their S and O columns, running max, row
         // sums and P entries, so the two groups never wait for each other.
         constexpr int RH = C::kRH;
@@ -1058,24 +1062,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                     for (int c = 0; c < RH; c += kLd)
                         tmem_ld32<kLd>(s_col + c, x[hf] + c);
                 }
-                if constexpr (C::kStackQ) {
-                    float y[NH][RH];
-#pragma unroll
-                    for (int hf = 0; hf < NH; ++hf) {
-                        const uint32_t s_col = tmem_s0 + sb * C::kSBufCols + hf * C::kSCols + RP + r0 + lane_off;
-#pragma unroll
-                        for (int c = 0; c < RH; c += kLd)
-                            tmem_ld32<kLd>(s_col + c, y[hf] + c);
-                    }
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int hf = 0; hf < NH; ++hf)
-#pragma unroll
-                        for (int r = 0; r < RH; ++r)
-                            x[hf][r] += y[hf][r];
-                } else {
-                    tmem_wait_ld();
-                }
+                tmem_wait_ld();
             }
             tc_fence_before();
             __syncwarp();
@@ -1142,7 +1129,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                     alpha_s[rg] = (mo == -CUDART_INF_F) ? 0.f : exp2f(mo - mn);
                     m_run[rg] = mn;
                     m_thr[rg] = mn + C::kThrLog2;
-                    m_sub[rg] = mn == -CUDART_INF_F ? 0.f : mn - (float)C::kPShift;
+                    m_sub[rg] = mn == -CUDART_INF_F ? 0.f : mn;
                 }
                 named_bar_sync(bar_id, 128);
 #pragma unroll
@@ -1181,9 +1168,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             if (!failed) {
                 // probabilities against the running max (masked entries are -inf -> 0), written as
                 // this token's row of P^T over the tile's K area, which QK(j) no longer needs:
-                // MN-major, 128-byte swizzle, 16-byte unit u of row t stored at u ^ (t % 8).
-                // bf16: row r at bytes [2r, 2r + 2).  fp8: p * 2^kPShift = hi + lo, two e4m3 codes
-                // at bytes r and RP + r.
+                // MN-major, 128-byte swizzle, 16-byte unit u of row t stored at u ^ (t % 8); row r
+                // at bytes [2r, 2r + 2).
                 // The group's running maxima are read before the first P store: the compiler cannot
                 // tell the stores from these shared-memory words, so a read after a store would
                 // wait for it (1-2 us per call on the large batches).
@@ -1200,11 +1186,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                 for (int hf = 0; hf < NH; ++hf) {
                     const int t = hf * kTokTile + tau;          // token of the tile
                     uint8_t *prow = smem + st * C::kStageBytes + (t >> 3) * C::kGroupBytes + (t & 7) * 128;
-                    uint2 hprev = make_uint2(0u, 0u), lprev = make_uint2(0u, 0u);
 #pragma unroll
                     for (int u = 0; u < RH / 8; ++u) {
                         const float *mm = msub + 8 * u;
-                        uint32_t pk[4], hc[4], lc[4];
+                        uint32_t pk[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const int r = 8 * u + 2 * e;
@@ -1212,55 +1197,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                             const float p1 = ex2_ftz(x[hf][r + 1] - mm[2 * e + 1]);
                             lsum[r] += p0;
                             lsum[r + 1] += p1;
-                            if constexpr (FP8) {
-                                // hi: p cut to 3 fraction bits (an e4m3 value when p >= 2^-6, else
-                                // rounded to the e4m3 subnormal grid, 2^-10 off at most); lo: the
-                                // exact f32 remainder, rounded to e4m3
-                                const float h0 = __uint_as_float(__float_as_uint(p0) & 0xFFF00000u);
-                                const float h1 = __uint_as_float(__float_as_uint(p1) & 0xFFF00000u);
-                                hc[e] = pack_e4m3x2(h0, h1);
-                                lc[e] = pack_e4m3x2(p0 - h0, p1 - h1);
-                            } else {
-                                pk[e] = pack_bf16x2(p0, p1);
-                            }
+                            pk[e] = pack_bf16x2(p0, p1);
                         }
-                        if constexpr (FP8) {
-                            // 8 rows' hi and lo codes; with 16 rows per group they leave as two
-                            // 16-byte stores per 16 rows (one per term), else as 8-byte stores
-                            const uint2 h2 = make_uint2(hc[0] | (hc[1] << 16), hc[2] | (hc[3] << 16));
-                            const uint2 l2 = make_uint2(lc[0] | (lc[1] << 16), lc[2] | (lc[3] << 16));
-                            if constexpr (RH % 16 == 0) {
-                                if ((u & 1) == 0) {
-                                    hprev = h2;
-                                    lprev = l2;
-                                } else {
-                                    const int bh = r0 + 8 * (u - 1), bl = RP + bh;   // multiples of 16
-                                    *reinterpret_cast<uint4 *>(prow + (((bh >> 4) ^ (t & 7)) << 4)) =
-                                        make_uint4(hprev.x, hprev.y, h2.x, h2.y);
-                                    *reinterpret_cast<uint4 *>(prow + (((bl >> 4) ^ (t & 7)) << 4)) =
-                                        make_uint4(lprev.x, lprev.y, l2.x, l2.y);
-                                }
-                            } else {
-                                const int bh = r0 + 8 * u, bl = RP + r0 + 8 * u;     // byte of the first row
-                                *reinterpret_cast<uint2 *>(prow + (((bh >> 4) ^ (t & 7)) << 4) + (bh & 15)) = h2;
-                                *reinterpret_cast<uint2 *>(prow + (((bl >> 4) ^ (t & 7)) << 4) + (bl & 15)) = l2;
-                            }
-                        } else {
-                            const int ug = r0 / 8 + u;                 // unit of the row
-                            *reinterpret_cast<uint4 *>(prow + ((ug ^ (t & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                        }
+                        const int ug = r0 / 8 + u;                     // unit of the row
+                        *reinterpret_cast<uint4 *>(prow + ((ug ^ (t & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                     }
                     const int tok = k0 + j * C::kTile + t;
                     if (tok >= w.L && tok < last_page_end) {
                         // past L in the last page the row holds anything (0 * NaN would reach O): this
-                        // group's share of the token's V row becomes zeros (bf16: chunk 2 + wg; fp8: a
-                        // half or a quarter of the 128 code bytes)
-                        static_assert(FP8 || C::kGroups == 2, "bf16 V rows are zeroed by chunk");
-                        constexpr int kZeroBytes = FP8 ? 128 / C::kGroups : 128;
+                        // group's share of the token's V row becomes zeros (chunk 2 + wg)
+                        static_assert(C::kGroups == 2, "bf16 V rows are zeroed by chunk");
                         uint8_t *vrow = smem + st * C::kStageBytes + C::kOffV + (t >> 3) * C::kGroupBytes + (t & 7) * 128 +
-                                        wg * (FP8 ? kZeroBytes : 1024);
+                                        wg * 1024;
 #pragma unroll
-                        for (int u = 0; u < kZeroBytes / 16; ++u)
+                        for (int u = 0; u < 128 / 16; ++u)
                             *reinterpret_cast<uint4 *>(vrow + u * 16) = make_uint4(0u, 0u, 0u, 0u);
                     }
                 }
@@ -1304,22 +1254,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             // dimensions of each row); the rows' slots were computed during the set-up
             if (ntiles > 0)
                 tc_fence_after();
-            const float o_scale = p.v_scale * (1.0f / (float)(1 << C::kPShift));
 #pragma unroll
             for (int c = 0; c < RH; c += kLd) {
                 float o[kLd];
                 if (ntiles > 0) {
                     tmem_ld32<kLd>(tmem_o + r0 + c + lane_off, o);
-                    if constexpr (FP8) {
-                        float o2[kLd];
-                        tmem_ld32<kLd>(tmem_o + RP + r0 + c + lane_off, o2);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int r = 0; r < kLd; ++r)
-                            o[r] += o2[r];
-                    } else {
-                        tmem_wait_ld();
-                    }
+                    tmem_wait_ld();
                 } else {
 #pragma unroll
                     for (int r = 0; r < kLd; ++r)
@@ -1328,7 +1268,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                 const long long *slots = reinterpret_cast<const long long *>(misc + C::kSlot);
 #pragma unroll
                 for (int rr = 0; rr < kLd; ++rr)
-                    o[rr] = alpha_s[r0 + c + rr] > 0.f ? o[rr] * o_scale : 0.f;
+                    o[rr] = alpha_s[r0 + c + rr] > 0.f ? o[rr] : 0.f;
                 // 4 x 4 transposes within lane quads: lane 4a + b ends with row 4k + b of each block of
                 // four rows and dimensions 4a .. 4a + 3 of the warp's quarter, so a warp store writes
                 // four rows of 128 contiguous bytes, 16 bytes a lane (part_o is 16-byte aligned)
@@ -1355,7 +1295,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             const int r = r0 + tid;
             if (tid < RH && r < R) {
                 const long long slot = reinterpret_cast<const long long *>(misc + C::kSlot)[r];
-                const float l = alpha_s[r] * (1.0f / (float)(1 << C::kPShift));
+                const float l = alpha_s[r];
                 p.part_m[slot] = l > 0.f ? m_run[r] * 0.69314718055994531f : -CUDART_INF_F;
                 p.part_l[slot] = l;
             }
