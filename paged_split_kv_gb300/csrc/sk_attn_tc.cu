@@ -143,9 +143,15 @@ struct Cfg {
     static constexpr int kPShift = FP8 ? 4 : 0;
     static_assert(kPShift >= 0 && kPShift < 8, "P * 2^kPShift stays inside the e4m3 range");
     // misc area
-    static constexpr int kBarFull = 0;                       // [kStages]
-    static constexpr int kBarEmpty = 8 * kStages;            // [kStages]
-    static constexpr int kBarSFull = 16 * kStages;           // [kSBufs]
+    // Landing barriers per stage: one per 128-token half for e4m3 with up to 32 rows, where QK runs
+    // ahead of the softmax (two S buffers) and so waits for copies: the first half's products go
+    // out while the second half lands (draft-extend workload 194.0 -> 192.8 us per step).  With
+    // 64 rows QK waits for the single S buffer instead, and a second check only cost time
+    // (179.5 -> 182.9 us).
+    static constexpr int kLand = (FP8 && RP <= 32) ? kHalves : 1;
+    static constexpr int kBarFull = 0;                       // [kStages][kLand]: (a half of) the tile landed
+    static constexpr int kBarEmpty = 8 * kStages * kLand;    // [kStages]
+    static constexpr int kBarSFull = kBarEmpty + 8 * kStages; // [kSBufs]
     static constexpr int kBarSFree = kBarSFull + 8 * kSBufs; // [kSBufs]
     static constexpr int kBarPFull = kBarSFree + 8 * kSBufs; // [kStages], by stage
     static constexpr int kBarODone = kBarPFull + 8 * kStages; // committed once, after the last PV
@@ -360,7 +366,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
     float *m_sub = reinterpret_cast<float *>(misc + C::kMsub);
     float *alpha_s = reinterpret_cast<float *>(misc + C::kAlpha);
     float *crow = reinterpret_cast<float *>(misc + C::kCrow);
-    auto bar_full = [&](int s) { return mbase + C::kBarFull + 8 * s; };
+    auto bar_full = [&](int s, int hf) { return mbase + C::kBarFull + 8 * (s * C::kLand + hf); };
     auto bar_empty = [&](int s) { return mbase + C::kBarEmpty + 8 * s; };
     auto bar_sfull = [&](int b) { return mbase + C::kBarSFull + 8 * b; };
     auto bar_sfree = [&](int b) { return mbase + C::kBarSFree + 8 * b; };
@@ -422,7 +428,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
     }
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(bar_full(s), 1);
+            for (int hf = 0; hf < C::kLand; ++hf)
+                mbar_init(bar_full(s, hf), 1);
             mbar_init(bar_empty(s), 1);
             mbar_init(bar_pfull(s), C::kSoftmaxWarps);
         }
@@ -540,7 +547,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
             q_blk[C::kStages - 1] = (lane < C::kPagesPerTile && j + C::kStages < ntiles && pg_far < page_end)
                                         ? __ldg(bt_row + pg_far) : -1;
             if (lane == 0)
-                mbar_arrive_expect_tx(bar_full(st), C::kTxBytes);
+                for (int hf = 0; hf < C::kLand; ++hf)
+                    mbar_arrive_expect_tx(bar_full(st, hf), C::kTxBytes / C::kLand);
             __syncwarp();
             if (lane < C::kPagesPerTile) {
                 int grp = -2;                         // whole box out of bounds: zero fill
@@ -550,7 +558,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                     else
                         atomicOr(p.status, SK_DEV_BAD_BLOCK);
                 }
-                tma_load_4d(stage(st) + lane * C::kPageBytes, &kv_map, 0, 0, 0, grp, bar_full(st));
+                tma_load_4d(stage(st) + lane * C::kPageBytes, &kv_map, 0, 0, 0, grp,
+                            bar_full(st, lane / (C::kPagesPerTile / C::kLand)));
                 // bf16: tile j + 1 goes to L2 now, so that its copy into a stage, which waits for a
                 // stage to free, mostly hits L2 (one tile more in flight than the stages hold).
                 // (fp8's 256-token tiles were measured slower with it: 198 -> 208 us on a 1.19 GB batch.)
@@ -573,7 +582,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
         // reused; each of the last kStages tiles is the last phase its barrier will see, so these
         // waits are unambiguous and return at once when the consumers already saw them land.
         for (int t = issued > C::kStages ? issued - C::kStages : 0; t < issued; ++t)
-            mbar_wait_bounded(bar_full(t % C::kStages), (t / C::kStages) & 1, nullptr, kDrainLimit);
+            for (int hf = 0; hf < C::kLand; ++hf)
+                mbar_wait_bounded(bar_full(t % C::kStages, hf), (t / C::kStages) & 1, nullptr, kDrainLimit);
     } else if (warp == 1 || warp == C::kPvWarp) {
         // ================================================================ MMA issuers
         // Whole warps run these loops; one elected lane issues each MMA and commit.
@@ -603,15 +613,26 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p)
                 const int st = j % C::kStages, b = j % C::kSBufs;
                 if (j >= C::kSBufs)
                     ok = mbar_wait_bounded(bar_sfree(b), ((j / C::kSBufs) - 1) & 1, abort_flag, p.wait_limit);
-                if (ok)
-                    ok = mbar_wait_bounded(bar_full(st), (j / C::kStages) & 1, abort_flag, p.wait_limit);
+                if constexpr (C::kLand == 1) {
+                    if (ok)
+                        ok = mbar_wait_bounded(bar_full(st, 0), (j / C::kStages) & 1, abort_flag, p.wait_limit);
+                }
                 ok = __all_sync(kFull, ok);
                 if (!ok)
                     break;
-                tc_fence_after();
+                if constexpr (C::kLand == 1)
+                    tc_fence_after();
 #pragma unroll
-                for (int hf = 0; hf < C::kHalves; ++hf) {
-                    // half hf: tokens [128 hf, 128 hf + 128) of the tile, 16 groups further on
+                for (int hf = 0; hf < C::kHalves && ok; ++hf) {
+                    // half hf: tokens [128 hf, 128 hf + 128) of the tile, 16 groups further on; with a
+                    // landing barrier per half, its products go out as soon as its pages have landed
+                    if constexpr (C::kLand > 1) {
+                        ok = __all_sync(kFull, mbar_wait_bounded(bar_full(st, hf), (j / C::kStages) & 1, abort_flag,
+                                                                 p.wait_limit));
+                        if (!ok)
+                            break;
+                        tc_fence_after();
+                    }
                     const uint32_t so = (uint32_t)(st * C::kStageBytes + hf * 16 * C::kGroupBytes);
                     const uint32_t sd = tmem_s0 + b * C::kSBufCols + hf * C::kSCols;
                     if constexpr (C::kStackQ) {
