@@ -83,6 +83,8 @@ plan_kernel(const int32_t *__restrict__ seq_lens, const int32_t *__restrict__ cu
         cu_a = __ldg(cu_q + tid);
         cu_b = __ldg(cu_q + tid + 1);
     }
+    // the ends of cu_seqlens_q for the coverage check at the end, loaded with everything else
+    const int cu_first = __ldg(cu_q), cu_last = __ldg(cu_q + bs);
 
     // 1. tile counts; largest, number of non-empty sequences, total
     long long my_max = 0, my_nonempty = 0, my_sum = 0;
@@ -229,7 +231,7 @@ plan_kernel(const int32_t *__restrict__ seq_lens, const int32_t *__restrict__ cu
     // outside [cu[0], cu[bs]) belong to no sequence; they get 0 segments (the merge writes 0 for
     // them), and the status word reports the inconsistency.
     {
-        const int first = __ldg(cu_q), last = __ldg(cu_q + bs);
+        const int first = cu_first, last = cu_last;
         if (tid == 0 && (first != 0 || last != num_tokens))
             atomicOr(status, SK_DEV_BAD_SEQ);
         const int lo_end = min(max(first, 0), num_tokens), hi_begin = min(max(last, 0), num_tokens);
