@@ -166,13 +166,18 @@ def test_fixed_split_reports_query_offsets_that_do_not_cover_the_tokens():
     assert run_library(pr, q, kv, use_plan=False).status == 0
 
 
-def test_bounded_wait_that_expires_is_reported_and_the_context_stays_usable():
+@pytest.mark.parametrize("hq, kv_dtype", [(32, si.KV_BF16), (16, si.KV_FP8), (32, si.KV_FP8)])
+def test_bounded_wait_that_expires_is_reported_and_the_context_stays_usable(hq, kv_dtype):
     """The timeout path in an unchanged kernel: a wait limit of 0 cycles makes the
     attention kernel's abortable waits give up as soon as a copy or product is not
     already complete.  Every CTA then drains what it issued and exits; the status
     word carries SK_DEV_TIMEOUT, the C call reports SK_ERR_TIMEOUT, and the next
-    call with the default limit is clean and bit-identical to one made before."""
-    w = si.make_workload("timeout_4x60000_q4", [60000] * 4, 4, 32, 2, seed=59)
+    call with the default limit is clean and bit-identical to one made before.
+    Three kernel shapes: bf16 with 64 rows; e4m3 with 32 rows (a landing barrier per
+    128-token half); e4m3 with 64 rows (four softmax groups, one S buffer)."""
+    fp8 = kv_dtype == si.KV_FP8
+    w = si.make_workload("timeout_4x60000_q4", [60000] * 4, 4, hq, 2, seed=59, kv_dtype=kv_dtype,
+                         k_scale=0.5 if fp8 else 1.0, v_scale=0.25 if fp8 else 1.0)
     q = si.make_q(w, D)
     kv = si.make_kv(w, D)
     before = run_library(w, q, kv)
@@ -186,19 +191,19 @@ def test_bounded_wait_that_expires_is_reported_and_the_context_stays_usable():
         bt = torch.as_tensor(w.block_table, device=D)
         plan = torch.empty(sk.plan_capacity(w.bs, 2, 148), dtype=torch.int32, device=D)
         tok = torch.empty(w.num_tokens, dtype=torch.int32, device=D)
-        po, pm, pl = _partials(w.num_tokens, 32)
+        po, pm, pl = _partials(w.num_tokens, hq)
         sk.sk_plan_cache_reset()
         sk.sk_build_plan(lens, cu, 2, plan, tok, 148, 64)
         for _ in range(3):                       # the calls return; nothing hangs
             sk.sk_paged_decode_attn(q, kv, bt, lens, cu, plan, po, pm, pl, max_q_len=4,
-                                    sm_scale=w.sm_scale, num_sms=148)
+                                    sm_scale=w.sm_scale, num_sms=148, k_scale=w.k_scale, v_scale=w.v_scale)
         rc = lib.sk_get_device_status(None, 1)
         assert rc == sk.SK_ERR_TIMEOUT, rc
         assert lib.sk_last_device_status() & sk.SK_DEV_TIMEOUT
         assert b"expired" in lib.sk_last_error()
         # the binding returns the mask, timeout bit included
         sk.sk_paged_decode_attn(q, kv, bt, lens, cu, plan, po, pm, pl, max_q_len=4, sm_scale=w.sm_scale,
-                                num_sms=148)
+                                num_sms=148, k_scale=w.k_scale, v_scale=w.v_scale)
         assert sk.sk_get_device_status(clear=True) & sk.SK_DEV_TIMEOUT
     finally:
         sk.sk_set_wait_limit(-1)
