@@ -21,6 +21,8 @@
 //            segment end are out-of-bounds boxes: zero-filled, no HBM traffic.
 //            It starts as soon as the mbarriers exist, with the block ids of
 //            its first tiles already read; later it reads them a ring ahead.
+//            On e4m3 pages with up to 32 rows each 128-token half of a tile
+//            lands on its own barrier, so QK starts on the first half.
 //   warp 1   allocates TMEM; issues the QK products.
 //   warp 10 (18)  issues the PV products.  Both issuers run converged and issue
 //            through one elected lane, so the descriptors stay warp-uniform.
